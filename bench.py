@@ -1,0 +1,470 @@
+"""Benchmark of the multi-LoRA MoE adapter path on one GB300 (per rank).
+
+One step = one pass of the whole path over one batch: moe_lora_align followed
+by moe_lora_fused_shrink_expand (add_inputs=1).  The metric is microseconds
+per step (lower is better); the default workload is the decode Qwen3-MoE-30B-A3B
+w13 LoRA shape (M=16, K=2048, N=1536, E=128, topk=8, max_loras=4 with 2
+active, r=16, block_size=16, Zipf(1.1) routing), inputs synthetic and seeded.
+
+Timing: inputs are resident in HBM; NB rotating copies of every input whose
+total footprint exceeds 3x L2 are cycled so that no step finds its operands in
+L2; W untimed warm-up steps; then exactly K steps replayed from CUDA graphs,
+bracketed by a barrier and a device synchronisation, timed with CUDA events on
+the launching stream; the max over ranks is reported.  Kernel-level durations
+(align alone, fused alone) are taken the same way for the roofline entry.
+
+Launch under torchrun for N > 1: every rank runs its own replica (the path has
+no exchange step); rank 0 prints the JSON line.
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+instead, on a bounded sample of pairs per step, scaled to microseconds per
+full step.
+"""
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from lora_moe_gb300 import inputs as gen  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode_qwen3_w13"
+METRIC = "fused MoE-LoRA us/call (align + fused shrink/expand step)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200000)
+    ap.add_argument("--warmup", type=int, default=2000)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernel-seconds", type=float, default=0.3,
+                    help="device time spent on each kernel-level timing")
+    return ap.parse_args()
+
+
+# --------------------------------------------------------------------------- roofline bookkeeping
+
+def algorithmic_counts(inp: gen.Inputs):
+    """What the method must move / compute for one step, from the actual inputs.
+
+    bytes = x rows of covered tokens once + A and B of every touched (lora,
+    expert) segment once + y read and write of covered pairs + align metadata;
+    flops = 2 r (K + N) per covered pair."""
+    w = inp.w
+    act = set(int(v) for v in inp.lora_ids)
+    m_cov = np.array([int(l) in act for l in inp.token_lora_mapping])
+    pairs = [(int(inp.token_lora_mapping[m]), int(inp.topk_ids[m, k]))
+             for m in range(w.M) if m_cov[m] for k in range(w.topk)]
+    P = len(pairs)
+    segs = {}
+    for le in pairs:
+        segs[le] = segs.get(le, 0) + 1
+    S = len(segs)
+    padded = sum(-(-c // w.block_size) * w.block_size for c in segs.values())
+    blocks = padded // w.block_size
+    r = w.rank
+    fused_bytes = (2 * w.K * int(m_cov.sum()) + S * 2 * r * (w.K + w.N) + P * w.N * 2 * 2
+                   + 4 * (padded + blocks + w.num_active_loras))
+    align_bytes = 4 * w.M * w.topk + 4 * w.M + 4 * (padded + blocks + w.num_active_loras)
+    return dict(pairs=P, segments=S, padded_rows=padded, blocks=blocks, fused_bytes=fused_bytes,
+                align_bytes=align_bytes, flops=2 * r * (w.K + w.N) * P)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while active."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        samples = []
+        for _, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                samples.append(dict(sm=float(parts[1]), sm_max=float(parts[2]),
+                                    reasons=dict(hw_slowdown=parts[5], hw_thermal_slowdown=parts[6],
+                                                 sw_thermal_slowdown=parts[7], sw_power_cap=parts[8])))
+            except ValueError:
+                continue
+        if not samples:
+            return None
+        reasons = sorted({k for s in samples for k, v in s["reasons"].items() if v.lower() == "active"})
+        return {"sm_mhz": float(np.median([s["sm"] for s in samples])),
+                "sm_max_mhz": max(s["sm_max"] for s in samples),
+                "reasons": reasons, "samples": len(samples)}
+
+
+# --------------------------------------------------------------------------- distributed plumbing
+
+def dist_setup(use_cuda):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if use_cuda else "gloo")
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg, use_cuda):
+    if pg is not None:
+        if use_cuda:
+            import torch
+            pg.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, value, use_cuda):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device="cuda" if use_cuda else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+
+def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: int = None):
+    """Time the oracle's align (whole batch) and fused stage (a rotating subset
+    of covered pairs, every column) and scale to microseconds per full step.
+
+    Returns (us_per_step, description, calls_made)."""
+    import oracle
+    w = inp.w
+    act = set(int(v) for v in inp.lora_ids)
+    cov = np.array([int(inp.token_lora_mapping[f // w.topk]) in act for f in range(w.M * w.topk)])
+    cov_idx = np.flatnonzero(cov).astype(np.int32)
+    cols = np.arange(w.N, dtype=np.int32)
+    n = max(1, min(pairs_per_call, len(cov_idx)))
+    t_align = t_fused = 0.0
+    done_pairs = 0
+    made = 0
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.align(inp.topk_ids, inp.token_lora_mapping, inp.lora_ids, w.E, w.max_loras, w.block_size)
+        t1 = time.perf_counter()
+        sel = cov_idx[(made * n + np.arange(n)) % max(1, len(cov_idx))] if len(cov_idx) else cov_idx
+        if len(sel):
+            oracle.fused_sampled(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
+                                 inp.lora_ids, sel, cols)
+        t2 = time.perf_counter()
+        t_align += t1 - t0
+        t_fused += t2 - t1
+        done_pairs += len(sel)
+        made += 1
+        if calls is not None:
+            if made >= calls:
+                break
+        elif time.perf_counter() - t_start >= budget_s:
+            break
+    per_pair = t_fused / max(1, done_pairs)
+    us = (t_align / made + per_pair * len(cov_idx)) * 1e6
+    desc = ("oracle align over the whole batch + oracle fused over %d of %d covered pairs per call "
+            "(all %d columns), %d calls, scaled to one full step" % (n, len(cov_idx), w.N, made))
+    return us, desc, made
+
+
+# --------------------------------------------------------------------------- GPU side
+
+def run_ours(args, world, rank, local, pg):
+    import torch
+    from lora_moe_gb300 import binding as B
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = gen.WORKLOADS[args.workload]
+    inp = gen.make_inputs(w)
+    counts = algorithmic_counts(inp)
+
+    def i32(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    per_set = (inp.x.nbytes + inp.lora_a.nbytes + inp.lora_b.nbytes + 2 * inp.y_in.nbytes +
+               inp.topk_ids.nbytes + inp.token_lora_mapping.nbytes)
+    NB = int(max(2, min(64, -(-3 * l2 // per_set))))
+    base = dict(topk_ids=i32(inp.topk_ids), mapping=i32(inp.token_lora_mapping), lora_ids=i32(inp.lora_ids),
+                x=bf16(inp.x), a=bf16(inp.lora_a), b=bf16(inp.lora_b), y=bf16(inp.y_in))
+    sets = []
+    for i in range(NB):
+        s = {k: v.clone() for k, v in base.items()}
+        s["buf"] = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size, device=dev)
+        sets.append(s)
+    del base
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    variant_ws = sets[0]["buf"].workspace is not None
+    align_launches = 3 if variant_ws else 1
+
+    def align(s):
+        b = s["buf"]
+        B.moe_lora_align(s["topk_ids"], s["mapping"], s["lora_ids"], w.E, w.max_loras, w.block_size,
+                         b.sorted_token_ids, b.expert_ids, b.num_tokens_post_padded, workspace=b.workspace,
+                         err_flag=err, stream=stream)
+
+    def fused(s):
+        b = s["buf"]
+        B.moe_lora_fused_shrink_expand(s["x"], s["a"], s["b"], s["y"], b.sorted_token_ids, b.expert_ids,
+                                       b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
+                                       add_inputs=True, err_flag=err, stream=stream)
+
+    def step(i):
+        s = sets[i % NB]
+        align(s)
+        fused(s)
+
+    def capture(fn, n):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    fn(i)
+        return g
+
+    # warm-up (also primes every set's align output for the fused-only timing)
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, NB)):
+            step(i)
+    stream.synchronize()
+    assert int(err.item()) == 0, "device error flag %d" % int(err.item())
+
+    g_round = capture(step, NB)
+    rem = args.steps % NB
+    g_rem = capture(step, rem) if rem else None
+    stream.synchronize()
+
+    # ---------------- timed region: exactly K steps
+    sampler = ClockSampler(local)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    barrier(pg, True)
+    torch.cuda.synchronize()
+    sampler.start()
+    e0.record(stream)
+    for _ in range(args.steps // NB):
+        g_round.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    barrier(pg, True)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms = max_over_ranks(pg, ms, True)
+    assert int(err.item()) == 0, "device error flag %d" % int(err.item())
+
+    # ---------------- kernel-level timing (each kernel alone, same rotation)
+    def kernel_time(fn, launches_per_call):
+        g = capture(lambda i: fn(sets[i % NB]), NB)
+        g.replay()
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        stream.synchronize()
+        one = max(1e-6, a.elapsed_time(b))
+        reps = max(1, int(args.kernel_seconds * 1e3 / one))
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        stream.synchronize()
+        return a.elapsed_time(b) * 1e3 / (reps * NB)   # us per call
+
+    fused_us = kernel_time(fused, 1)
+    align_us = kernel_time(align, align_launches)
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = dict(topk_ids=torch.from_numpy(inp.topk_ids).pin_memory(),
+                    mapping=torch.from_numpy(inp.token_lora_mapping).pin_memory(),
+                    lora_ids=torch.from_numpy(inp.lora_ids).pin_memory(),
+                    x=torch.from_numpy(inp.x.view(np.int16)).pin_memory(),
+                    y=torch.from_numpy(inp.y_in.view(np.int16)).pin_memory())
+        out_host = torch.empty(inp.y_in.shape, dtype=torch.int16).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+        n_e2e = max(3, min(args.steps, 2000))
+
+        def e2e_step(i):
+            s = sets[i % NB]
+            with torch.cuda.stream(stream):
+                s["topk_ids"].copy_(host["topk_ids"], non_blocking=True)
+                s["mapping"].copy_(host["mapping"], non_blocking=True)
+                s["lora_ids"].copy_(host["lora_ids"], non_blocking=True)
+                s["x"].view(torch.int16).copy_(host["x"], non_blocking=True)
+                s["y"].view(torch.int16).copy_(host["y"], non_blocking=True)
+            align(s)
+            fused(s)
+            with torch.cuda.stream(stream):
+                out_host.copy_(s["y"].view(torch.int16), non_blocking=True)
+
+        for i in range(3):
+            e2e_step(i)
+        stream.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        barrier(pg, True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for i in range(n_e2e):
+            e2e_step(i)
+        b.record(stream)
+        stream.synchronize()
+        e2e_ms = max_over_ranks(pg, a.elapsed_time(b), True)
+        e2e = {"value": e2e_ms * 1e3 / (n_e2e * world), "unit": "us/call", "steps": n_e2e,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+    peak, peak_kind = measured_peaks()
+    achieved = counts["fused_bytes"] / (fused_us * 1e-6) / 1e9
+    return dict(ms=ms, clocks=clocks, fused_us=fused_us, align_us=align_us, counts=counts, NB=NB, l2=l2,
+                footprint=NB * per_set,
+                align_launches=align_launches, e2e=e2e, achieved=achieved, peak=peak, peak_kind=peak_kind,
+                inp=inp)
+
+
+def main():
+    args = parse()
+    if args.steps < 1 or args.warmup < 3:
+        raise SystemExit("need --steps >= 1 and --warmup >= 3")
+    w = gen.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank != 0:
+            return
+        inp = gen.make_inputs(w)
+        # size the per-step sample so that W + K steps take a couple of minutes at most
+        probe_us, _, _ = time_oracle(inp, 0.5, 4)
+        per_pair_budget = 120.0 / (args.steps + args.warmup)
+        pairs_per_call = max(1, int(per_pair_budget / max(1e-9, probe_us * 1e-6 / max(1, algorithmic_counts(inp)["pairs"]))))
+        time_oracle(inp, 0, pairs_per_call, calls=args.warmup)
+        t0 = time.perf_counter()
+        us, desc, made = time_oracle(inp, 0, pairs_per_call, calls=args.steps)
+        wall = time.perf_counter() - t0
+        line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/call", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
+                "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "E": w.E, "topk": w.topk,
+                           "max_loras": w.max_loras, "num_active_loras": w.num_active_loras, "rank": w.rank,
+                           "block_size": w.block_size},
+                "cpu_baseline": {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": desc},
+                "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+                "wall_s": wall}
+        print(json.dumps(line))
+        return
+
+    import torch
+    world, rank, local, pg = dist_setup(True)
+    res = run_ours(args, world, rank, local, pg)
+    counts = res["counts"]
+    us_per_step = res["ms"] * 1e3 / (args.steps * world)
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        us, desc, made = time_oracle(res["inp"], 12.0, 8)
+        cpu = {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": desc}
+    if rank != 0:
+        if pg is not None:
+            pg.destroy_process_group()
+        return
+    line = {
+        "metric": METRIC, "value": us_per_step, "unit": "us/call", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (fp32 accumulate)",
+        "data": "synthetic (seeded numpy PCG64; random-init adapters, NaN-poisoned inactive slots)",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "E": w.E, "topk": w.topk,
+                   "max_loras": w.max_loras, "num_active_loras": w.num_active_loras, "rank": w.rank,
+                   "block_size": w.block_size, "add_inputs": 1, "parallelism": "replicas" if world > 1 else "single",
+                   "l2_policy": "%d rotating input sets, %.0f MB in total, L2 %.0f MB" % (
+                       res["NB"], res["footprint"] / 1e6, res["l2"] / 1e6),
+                   "timing": "CUDA graphs of align+fused steps, CUDA events on the launching stream"},
+        "kernels": {"align_us": res["align_us"], "fused_us": res["fused_us"],
+                    "align_launches_per_call": res["align_launches"],
+                    "fused_gbs": res["achieved"],
+                    "fused_tflops": counts["flops"] / (res["fused_us"] * 1e-6) / 1e12,
+                    "align_gbs": counts["align_bytes"] / (res["align_us"] * 1e-6) / 1e9},
+        "algorithmic": counts,
+        "roofline": {"bound": "hbm", "kernel": "fused_cuda_core_kernel" if w.M * w.topk < 1024 else
+                     "fused_tcgen05_kernel", "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s",
+                     "frac": res["achieved"] / res["peak"], "peak_kind": res["peak_kind"] + " (hbm_gbs)",
+                     "traffic": None},
+        "cpu_baseline": cpu,
+        "e2e": res["e2e"],
+        "gpu_launches": args.steps * (res["align_launches"] + 1),
+        "clocks": res["clocks"],
+    }
+    print(json.dumps(line))
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * moe_lora.h -- C ABI of the GB300 (sm_103a) multi-LoRA Mixture-of-Experts
+ * adapter library (libmoe_lora.so).
+ *
+ * Two stages make up the path:
+ *
+ *   moe_lora_align                 -- per active LoRA slot, group the
+ *       (token, top-k) pairs by expert into block_size-padded segments.
+ *       Defined by vLLM PR #29257 "Lora MoE Align Improvements", section
+ *       Purpose (a per-LoRA align kernel with a shared-memory variant and a
+ *       global-memory variant for large num_experts, sharing one align routine
+ *       with the non-LoRA case) and its review thread (token_lora_mapping dtype;
+ *       num_experts must not exceed 1024).  Output rows are per LoRA slot, as in
+ *       the `.view(max_loras, -1)` of sorted_token_ids / expert_ids in the test
+ *       diff of vLLM PR #32005 "Reduce the kernel overhead when num of active
+ *       loras is smaller than max loras", tests/lora/test_fused_moe_lora_kernel.py.
+ *
+ *   moe_lora_fused_shrink_expand   -- y[m,k,:] (+)= (x[m] . A[l,e]^T) . B[l,e]^T
+ *       with l = token_lora_mapping[m], e = topk_ids[m,k], the rank-r
+ *       intermediate never written to global memory.  Defined by the
+ *       prhub.com.cn summary of vLLM PR #42290 (one-shot fused MoE LoRA kernel
+ *       and dual-stream execution), sections "Features and motivation" and
+ *       "Implementation breakdown" step 1 (shrink and expand in one kernel, the
+ *       rank dimension kept on chip, add_inputs choosing accumulate or
+ *       overwrite) and "Key source snippets" (rank <= 128 for the one-shot
+ *       kernel).  The grid is sized by num_active_loras, not max_loras, as in
+ *       vLLM PR #32005, diff of vllm/lora/ops/triton_ops/fused_moe_lora_op.py
+ *       (_adjust_kernel_inputs).
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked [device] must be device pointers of the current CUDA
+ *     device; [host] are host pointers.  bf16 tensors are passed as
+ *     moe_lora_bf16 (raw IEEE bfloat16 bit patterns, uint16).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  Nothing is synchronised.
+ *   - The caller owns every buffer.  The library allocates no memory, keeps
+ *     no per-call state between calls and may be called from several host
+ *     threads.
+ *   - Return value: MOE_LORA_OK, or a moe_lora_status error code.  On an
+ *     argument error nothing is enqueued.  Errors the device detects
+ *     (out-of-range ids in device arrays, a wait that timed out) are OR-ed
+ *     as MOE_LORA_DEVERR_* bits into *err_flag (an int32 [device] word, may be
+ *     NULL), readable after the stream has synchronised; the offending entry is
+ *     skipped, never dereferenced.
+ *   - Every (token, top-k) pair is named by its flat index f = m*topk + k.
+ */
+#ifndef MOE_LORA_H
+#define MOE_LORA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t moe_lora_bf16;
+
+typedef enum {
+    MOE_LORA_OK = 0,
+    MOE_LORA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative or inconsistent size */
+    MOE_LORA_ERR_UNSUPPORTED = 2,   /* rank > 128, num_experts > 1024, bad block_size, ... */
+    MOE_LORA_ERR_MISALIGNED = 3,    /* a pointer or a row is not 16-byte aligned */
+    MOE_LORA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
+    MOE_LORA_ERR_LAUNCH = 5,        /* a CUDA launch or attribute call failed */
+    MOE_LORA_ERR_DEVICE = 6         /* no usable sm_100-family device is current */
+} moe_lora_status;
+
+/* Bits OR-ed into *err_flag by the kernels. */
+#define MOE_LORA_DEVERR_EXPERT_ID 0x1   /* topk_ids / expert_ids entry outside [0, num_experts) */
+#define MOE_LORA_DEVERR_LORA_ID 0x2     /* lora_ids entry outside [0, max_loras) */
+#define MOE_LORA_DEVERR_CAPACITY 0x4    /* align output larger than max_num_tokens_padded */
+#define MOE_LORA_DEVERR_PAIR_ID 0x8     /* sorted_token_ids entry neither a pair nor the sentinel */
+#define MOE_LORA_DEVERR_TIMEOUT 0x10    /* an on-chip wait gave up (a bounded wait ran out) */
+
+/* Align variants (moe_lora_align `variant`). */
+#define MOE_LORA_ALIGN_AUTO 0
+#define MOE_LORA_ALIGN_SMEM 1     /* one CTA per active slot, counters in shared memory */
+#define MOE_LORA_ALIGN_GLOBAL 2   /* many CTAs per slot, counters in the caller's workspace */
+
+/* Fused paths (moe_lora_fused_shrink_expand `path`). */
+#define MOE_LORA_PATH_AUTO 0
+#define MOE_LORA_PATH_CUDA_CORE 1 /* decode-sized blocks: CUDA cores, warp-shuffle reductions */
+#define MOE_LORA_PATH_TCGEN05 2   /* prefill-sized blocks: tcgen05 tensor-core MMAs */
+
+/* Capacity of one LoRA row of sorted_token_ids: every pair once plus up to
+ * block_size-1 padding slots for each expert: M*topk + num_experts*(block_size-1).
+ * Returns -1 on invalid sizes. */
+int moe_lora_max_num_tokens_padded(int M, int topk, int num_experts, int block_size);
+
+/* Capacity of one LoRA row of expert_ids: ceil(max_num_tokens_padded / block_size).
+ * Returns -1 on invalid sizes. */
+int moe_lora_max_num_m_blocks(int M, int topk, int num_experts, int block_size);
+
+/* Bytes of [device] workspace moe_lora_align needs for `variant` (0 for the
+ * shared-memory variant; for AUTO, the size of whichever variant AUTO picks for
+ * these sizes).  Returns 0 and the call needs no workspace when it is 0. */
+size_t moe_lora_align_workspace_bytes(int M, int topk, int num_experts,
+                                      int num_active_loras, int block_size, int variant);
+
+/*
+ * moe_lora_align -- group the pairs of each active LoRA slot by expert.
+ *
+ * For each z < num_active_loras, with l = lora_ids[z] (distinct, in
+ * [0, max_loras)):
+ *   cnt[e]  = number of pairs f with token_lora_mapping[f / topk] == l and
+ *             topk_ids[f] == e;
+ *   off[e]  = sum_{e' < e} ceil(cnt[e'] / block_size) * block_size;
+ *   num_tokens_post_padded[l] = off[num_experts];
+ *   sorted_token_ids[l][off[e] ...] = the pairs of expert e in ascending f,
+ *       followed by the sentinel M*topk up to the next multiple of block_size;
+ *   expert_ids[l][b] = e for every block b in [off[e], off[e+1]) / block_size.
+ * Experts with no pair get no block.  Tokens mapped to -1, or to a slot that
+ * is not in lora_ids, are dropped.  A slot whose adapter is disabled
+ * (adapter_enabled[l] == 0) gets num_tokens_post_padded[l] = 0.  Pairs whose
+ * expert is outside [0, num_experts) are dropped and flagged
+ * (MOE_LORA_DEVERR_EXPERT_ID).  Only num_tokens_post_padded[l] for active l,
+ * sorted_token_ids[l][0, ntpp) and expert_ids[l][0, ntpp / block_size) are
+ * written; every other entry keeps its previous contents.  The result is
+ * deterministic and identical for both variants.
+ *
+ *   topk_ids               [device] int32 [M, topk]
+ *   token_lora_mapping     [device] int32 [M], -1 = no adapter
+ *   lora_ids               [device] int32 [num_active_loras]
+ *   adapter_enabled        [device] int32 [max_loras], or NULL = all enabled
+ *   sorted_token_ids       [device] int32 [max_loras, max_num_tokens_padded]
+ *   expert_ids             [device] int32 [max_loras, max_num_m_blocks]
+ *   num_tokens_post_padded [device] int32 [max_loras]
+ *   workspace              [device] >= moe_lora_align_workspace_bytes(..., variant)
+ *                          bytes, 16-byte aligned; may be NULL when that is 0.
+ *                          Its contents need no initialisation and are
+ *                          overwritten.
+ * Sizes: 1 <= topk <= num_experts <= 1024; block_size in {16, 32, 64, 128};
+ * 0 <= num_active_loras <= max_loras; M >= 0 (M == 0 or num_active_loras == 0
+ * writes num_tokens_post_padded[l] = 0 for each listed slot, or nothing when
+ * the list is empty); max_num_tokens_padded / max_num_m_blocks must be at
+ * least the capacities returned above.
+ */
+int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping,
+                   const int32_t *lora_ids, const int32_t *adapter_enabled,
+                   int M, int topk, int num_experts, int max_loras,
+                   int num_active_loras, int block_size,
+                   int32_t *sorted_token_ids, int32_t *expert_ids,
+                   int32_t *num_tokens_post_padded,
+                   int max_num_tokens_padded, int max_num_m_blocks,
+                   void *workspace, size_t workspace_bytes,
+                   int variant, int32_t *err_flag, void *stream);
+
+/*
+ * moe_lora_fused_shrink_expand -- apply each covered pair's adapter.
+ *
+ * Reads the align outputs of the same slots and, for every block b of every
+ * active slot z (l = lora_ids[z], b < num_tokens_post_padded[l] / block_size)
+ * with e = expert_ids[l][b] and every pair f = sorted_token_ids[l][b*block_size + i]
+ * that is not the sentinel M*topk (m = f / topk):
+ *   t[j]      = sum_k x[m][k] * A[l][e][j][k]                 (j < rank, fp32)
+ *   y[f][n]   = bf16( (add_inputs ? y[f][n] : 0) + sum_j B[l][e][n][j] * t[j] )
+ * t stays in registers / shared memory / tensor memory.  Pairs of slots that
+ * are not listed, disabled, or not covered are not touched (in both modes).
+ * Tensor-core path: t is rounded to bf16 before the second product.
+ *
+ *   x                [device] bf16 [M, K] row-major
+ *   lora_a           [device] bf16 [max_loras, num_experts, rank, K]
+ *   lora_b           [device] bf16 [max_loras, num_experts, N, rank]
+ *   y                [device] bf16 [M, topk, N], read (if add_inputs) and written
+ *   sorted_token_ids, expert_ids, num_tokens_post_padded: as written by moe_lora_align
+ *                    with the same M, topk, num_experts, block_size and capacities
+ *   lora_ids         [device] int32 [num_active_loras]
+ *   adapter_enabled  [device] int32 [max_loras] or NULL
+ * Sizes: 1 <= rank <= 128 with rank % 4 == 0 (the tensor-core path needs
+ * rank % 8 == 0); K % 8 == 0 and N % 8 == 0; x, lora_a, lora_b, y 16-byte
+ * aligned; other limits as for moe_lora_align.  path: MOE_LORA_PATH_*; AUTO
+ * picks the CUDA-core path for decode-sized batches (M*topk < 1024) and the
+ * tensor-core path otherwise (when rank % 8 == 0).
+ */
+int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a,
+                                 const moe_lora_bf16 *lora_b, moe_lora_bf16 *y,
+                                 const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                                 const int32_t *num_tokens_post_padded,
+                                 const int32_t *lora_ids, const int32_t *adapter_enabled,
+                                 int M, int topk, int num_experts, int K, int N, int rank,
+                                 int max_loras, int num_active_loras, int block_size,
+                                 int max_num_tokens_padded, int max_num_m_blocks,
+                                 int add_inputs, int path, int32_t *err_flag, void *stream);
+
+/* Human-readable name of a moe_lora_status value (static string). */
+const char *moe_lora_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int moe_lora_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_LORA_H */

@@ -1,0 +1,159 @@
+"""Thin Python binding of libmoe_lora.so (include/moe_lora.h).
+
+Argument marshalling only: each function checks tensor dtypes / devices,
+passes raw pointers and sizes to the C ABI of the same name and raises
+MoeLoraError on a non-zero status.  Every step of the computation runs in
+the library's CUDA kernels; there is no other implementation to fall back to,
+so a missing library is an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+MOE_LORA_OK = 0
+ALIGN_AUTO, ALIGN_SMEM, ALIGN_GLOBAL = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TCGEN05 = 0, 1, 2
+DEVERR_EXPERT_ID, DEVERR_LORA_ID, DEVERR_CAPACITY, DEVERR_PAIR_ID, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
+
+_lib = None
+_lock = threading.Lock()
+
+
+class MoeLoraError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_string(status), status))
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libmoe_lora.so (building it with nvcc if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError("libmoe_lora.so is missing: " + path)
+            L = ctypes.CDLL(path)
+            I, P, S = ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+            L.moe_lora_version.restype = I
+            L.moe_lora_version.argtypes = []
+            L.moe_lora_status_string.restype = ctypes.c_char_p
+            L.moe_lora_status_string.argtypes = [I]
+            L.moe_lora_max_num_tokens_padded.restype = I
+            L.moe_lora_max_num_tokens_padded.argtypes = [I, I, I, I]
+            L.moe_lora_max_num_m_blocks.restype = I
+            L.moe_lora_max_num_m_blocks.argtypes = [I, I, I, I]
+            L.moe_lora_align_workspace_bytes.restype = S
+            L.moe_lora_align_workspace_bytes.argtypes = [I, I, I, I, I, I]
+            L.moe_lora_align.restype = I
+            L.moe_lora_align.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, I, I, P, S, I, P, P]
+            L.moe_lora_fused_shrink_expand.restype = I
+            L.moe_lora_fused_shrink_expand.argtypes = [P, P, P, P, P, P, P, P, P,
+                                                       I, I, I, I, I, I, I, I, I, I, I, I, I, P, P]
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_lora_status_string(int(status)).decode()
+
+
+def max_num_tokens_padded(M: int, topk: int, num_experts: int, block_size: int) -> int:
+    return lib().moe_lora_max_num_tokens_padded(M, topk, num_experts, block_size)
+
+
+def max_num_m_blocks(M: int, topk: int, num_experts: int, block_size: int) -> int:
+    return lib().moe_lora_max_num_m_blocks(M, topk, num_experts, block_size)
+
+
+def align_workspace_bytes(M, topk, num_experts, num_active_loras, block_size, variant=ALIGN_AUTO) -> int:
+    return lib().moe_lora_align_workspace_bytes(M, topk, num_experts, num_active_loras, block_size, variant)
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _check(status, what):
+    if status != MOE_LORA_OK:
+        raise MoeLoraError(status, what)
+
+
+def moe_lora_align(topk_ids, token_lora_mapping, lora_ids, num_experts, max_loras, block_size,
+                   sorted_token_ids, expert_ids, num_tokens_post_padded, adapter_enabled=None,
+                   workspace=None, variant=ALIGN_AUTO, err_flag=None, stream=None):
+    """moe_lora_align on device tensors; outputs are written in place."""
+    M, topk = topk_ids.shape
+    nact = lora_ids.numel()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = lib().moe_lora_align(
+        _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(token_lora_mapping, torch.int32, "token_lora_mapping"),
+        _ptr(lora_ids, torch.int32, "lora_ids"), _ptr(adapter_enabled, torch.int32, "adapter_enabled"),
+        M, topk, num_experts, max_loras, nact, block_size,
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(num_tokens_post_padded, torch.int32, "num_tokens_post_padded"),
+        sorted_token_ids.shape[-1], expert_ids.shape[-1],
+        _ptr(workspace, None, "workspace"), ws_bytes, variant,
+        _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+    _check(st, "moe_lora_align")
+
+
+def moe_lora_fused_shrink_expand(x, lora_a, lora_b, y, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                                 lora_ids, topk, block_size, add_inputs=True, adapter_enabled=None,
+                                 path=PATH_AUTO, err_flag=None, stream=None):
+    """moe_lora_fused_shrink_expand on device tensors; y is updated in place."""
+    M, K = x.shape
+    L, E, r, K2 = lora_a.shape
+    N = lora_b.shape[2]
+    if K2 != K or tuple(lora_b.shape) != (L, E, N, r) or y.numel() != M * topk * N:
+        raise ValueError("inconsistent shapes")
+    bf = torch.bfloat16
+    st = lib().moe_lora_fused_shrink_expand(
+        _ptr(x, bf, "x"), _ptr(lora_a, bf, "lora_a"), _ptr(lora_b, bf, "lora_b"), _ptr(y, bf, "y"),
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(num_tokens_post_padded, torch.int32, "num_tokens_post_padded"),
+        _ptr(lora_ids, torch.int32, "lora_ids"), _ptr(adapter_enabled, torch.int32, "adapter_enabled"),
+        M, topk, E, K, N, r, L, lora_ids.numel(), block_size,
+        sorted_token_ids.shape[-1], expert_ids.shape[-1], int(bool(add_inputs)), path,
+        _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+    _check(st, "moe_lora_fused_shrink_expand")
+
+
+class AlignBuffers:
+    """Device output buffers (and workspace) for one align configuration."""
+
+    def __init__(self, M, topk, num_experts, max_loras, num_active_loras, block_size, device="cuda",
+                 variant=ALIGN_AUTO):
+        cap = max_num_tokens_padded(M, topk, num_experts, block_size)
+        capb = max_num_m_blocks(M, topk, num_experts, block_size)
+        self.sorted_token_ids = torch.empty((max_loras, cap), dtype=torch.int32, device=device)
+        self.expert_ids = torch.empty((max_loras, capb), dtype=torch.int32, device=device)
+        self.num_tokens_post_padded = torch.empty((max_loras,), dtype=torch.int32, device=device)
+        nbytes = align_workspace_bytes(M, topk, num_experts, num_active_loras, block_size, variant)
+        self.workspace = torch.empty((max(nbytes, 16),), dtype=torch.uint8, device=device) if nbytes else None

@@ -1,0 +1,359 @@
+// align.cu -- moe_lora_align kernels for sm_103a.
+//
+// For each active LoRA slot the pairs f = m*topk + k of its tokens are counted
+// per expert, each count is padded to a multiple of block_size, the padded
+// counts are prefix-summed into segment offsets, and every pair is written to
+// its expert's segment in ascending f, padding slots holding the sentinel
+// M*topk (vLLM PR #29257 "Lora MoE Align Improvements", section Purpose: a
+// shared-memory variant, and a global-memory variant for large num_experts).
+//
+// Determinism without sorting: the pairs are split into contiguous per-warp
+// ranges.  A warp walks its range 32 pairs at a time; __match_any_sync groups
+// the lanes that hold the same expert, so a lane's rank among equal experts is
+// the popcount of the lower lanes in its group, and the group's size is added
+// to that warp's private counter for the expert.  A column scan over the warp
+// ranges (in range order) turns the counters into each warp's starting
+// position inside every segment, so the second walk scatters every pair to a
+// position that only depends on f -- the same result as a stable sort.
+//
+//   shared-memory variant : one CTA (32 warps) per active slot; the per-warp
+//                           counters live in shared memory.
+//   global-memory variant : many CTAs per slot; per-warp counters go to the
+//                           caller's workspace and three launches (count, scan,
+//                           scatter) replace the CTA-wide barriers.
+#include <cuda_runtime.h>
+
+#include "device_utils.cuh"
+#include "internal.h"
+
+namespace moe_lora {
+
+namespace {
+
+constexpr int kSmemWarps = 32;                  // shared-memory variant: warps per CTA
+constexpr int kSmemThreads = kSmemWarps * 32;
+constexpr int kGlobalWarpsPerCta = 8;           // global variant, count / scatter kernels
+constexpr int kGlobalThreads = kGlobalWarpsPerCta * 32;
+constexpr int kScanThreads = 1024;              // one thread per expert (E <= 1024)
+constexpr int kMaxGlobalWarpRanges = 128;       // global variant: target warp ranges per slot
+
+// Expert of pair f for slot l, or -1 when the pair is not this slot's or its
+// expert is out of range (flagged once, in the counting pass).
+__device__ __forceinline__ int pair_expert(const AlignArgs &a, int f, int l, bool flag) {
+  const int m = f / a.topk;
+  if (__ldg(a.token_lora_mapping + m) != l) return -1;
+  const int e = __ldg(a.topk_ids + f);
+  if (e < 0 || e >= a.num_experts) {
+    if (flag) flag_error(a.err, MOE_LORA_DEVERR_EXPERT_ID);
+    return -1;
+  }
+  return e;
+}
+
+// Slot z's LoRA index, or -1 when the slot is skipped (bad id: flagged;
+// disabled adapter: its num_tokens_post_padded is set to 0 by `writer`).
+__device__ __forceinline__ int slot_lora(const AlignArgs &a, int z, bool writer) {
+  const int l = __ldg(a.lora_ids + z);
+  if (l < 0 || l >= a.max_loras) {
+    if (writer) flag_error(a.err, MOE_LORA_DEVERR_LORA_ID);
+    return -1;
+  }
+  if (a.adapter_enabled && __ldg(a.adapter_enabled + l) == 0) {
+    if (writer) a.num_tokens_post_padded[l] = 0;
+    return -1;
+  }
+  return l;
+}
+
+// Walk [lo, hi) one warp-width at a time, adding group sizes to tab[e].
+__device__ __forceinline__ void warp_count(const AlignArgs &a, int l, int lo, int hi, int *tab,
+                                           int lane) {
+  for (int base = lo; base < hi; base += 32) {
+    const int f = base + lane;
+    const int e = (f < hi) ? pair_expert(a, f, l, true) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(peers) - 1) tab[e] += __popc(peers);
+  }
+}
+
+// Second walk: tab[e] holds this warp's next position in segment e.
+__device__ __forceinline__ void warp_scatter(const AlignArgs &a, int l, int lo, int hi, int *tab,
+                                             int32_t *sorted, int lane) {
+  const unsigned lower = (1u << lane) - 1u;
+  for (int base = lo; base < hi; base += 32) {
+    const int f = base + lane;
+    const int e = (f < hi) ? pair_expert(a, f, l, false) : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int pos = (e >= 0) ? tab[e] + __popc(peers & lower) : 0;
+    __syncwarp();
+    if (e >= 0) {
+      sorted[pos] = f;
+      if (lane == __ffs(peers) - 1) tab[e] += __popc(peers);
+    }
+    __syncwarp();
+  }
+}
+
+// Exclusive scan of one int per thread across a 1024-thread CTA; returns the
+// thread's exclusive prefix and writes the total to *total.
+__device__ __forceinline__ int block_exclusive_scan_1024(int v, int *warp_sums, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, s, d);
+      if (lane >= d) s += t;
+    }
+    warp_sums[lane] = s;
+  }
+  __syncthreads();
+  const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  *total = warp_sums[31];
+  return excl;
+}
+
+// Given per-expert counts cnt[e] (e < E, one per thread), compute segment
+// offsets off[0..E], write num_tokens_post_padded[l], the padding sentinels and
+// expert_ids.  Returns false (uniformly) when the result exceeds the caller's
+// capacity.  Called by all 1024 threads.
+__device__ bool write_segments(const AlignArgs &a, int l, const int *cnt, int *off, int *warp_sums) {
+  const int E = a.num_experts, bs = a.block_size, tid = threadIdx.x;
+  const int c = (tid < E) ? cnt[tid] : 0;
+  const int padded = (c + bs - 1) / bs * bs;
+  int total;
+  const int excl = block_exclusive_scan_1024(padded, warp_sums, &total);
+  if (tid < E) off[tid] = excl;
+  if (tid == 0) off[E] = total;
+  __syncthreads();
+  if (total > a.max_num_tokens_padded || total / bs > a.max_num_m_blocks) {
+    if (tid == 0) {
+      flag_error(a.err, MOE_LORA_DEVERR_CAPACITY);
+      a.num_tokens_post_padded[l] = 0;
+    }
+    return false;
+  }
+  if (tid == 0) a.num_tokens_post_padded[l] = total;
+  int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
+  int32_t *experts = a.expert_ids + (size_t)l * a.max_num_m_blocks;
+  const int sentinel = a.M * a.topk;
+  if (tid < E)
+    for (int i = excl + c; i < excl + padded; ++i) sorted[i] = sentinel;
+  const int nblocks = total / bs;
+  for (int b = tid; b < nblocks; b += blockDim.x) {
+    // the expert whose segment [off[e], off[e+1]) holds position b*bs
+    const int pos = b * bs;
+    int lo = 0, hi = E;   // invariant: off[lo] <= pos < off[hi]
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off[mid] <= pos) lo = mid; else hi = mid;
+    }
+    experts[b] = lo;
+  }
+  return true;
+}
+
+// ----------------------------------------------------- shared-memory variant
+
+__global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const AlignArgs a) {
+  extern __shared__ int smem[];
+  const int E = a.num_experts;
+  int *tab = smem;                          // [kSmemWarps][E] per-warp counters / cursors
+  int *cnt = tab + kSmemWarps * E;          // [E]
+  int *off = cnt + E;                       // [E + 1]
+  int *warp_sums = off + E + 1;             // [32]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  const int l = slot_lora(a, blockIdx.x, tid == 0);
+  if (l < 0) return;
+
+  for (int i = tid; i < kSmemWarps * E; i += kSmemThreads) tab[i] = 0;
+  __syncthreads();
+
+  const int P = a.M * a.topk;
+  const int per_warp = ((P + kSmemWarps - 1) / kSmemWarps + 31) / 32 * 32;
+  const int lo = min(P, warp * per_warp), hi = min(P, lo + per_warp);
+  int *mine = tab + warp * E;
+  warp_count(a, l, lo, hi, mine, lane);
+  __syncthreads();
+
+  // Column scan: each warp's starting position relative to its segment.
+  if (tid < E) {
+    int run = 0;
+    for (int w = 0; w < kSmemWarps; ++w) {
+      const int t = tab[w * E + tid];
+      tab[w * E + tid] = run;
+      run += t;
+    }
+    cnt[tid] = run;
+  }
+  __syncthreads();
+  if (!write_segments(a, l, cnt, off, warp_sums)) return;
+  if (tid < E)
+    for (int w = 0; w < kSmemWarps; ++w) tab[w * E + tid] += off[tid];
+  __syncthreads();
+
+  warp_scatter(a, l, lo, hi, mine,
+               a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded, lane);
+}
+
+// ----------------------------------------------------- global-memory variant
+// Workspace per slot z: hist[z] = int [W][E] (W warp ranges), then off[z] = int [E].
+
+struct GlobalLayout {
+  int pairs_per_warp;
+  int warps;  // W
+};
+
+__host__ __device__ inline size_t slot_stride_ints(int W, int E) { return (size_t)W * E + E; }
+
+__global__ void __launch_bounds__(kGlobalThreads) align_global_count_kernel(const AlignArgs a, int *ws,
+                                                                            GlobalLayout g) {
+  extern __shared__ int smem[];
+  const int E = a.num_experts;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int z = blockIdx.y;
+  const int l = slot_lora(a, z, false);
+  if (l < 0) return;
+  const int gw = blockIdx.x * kGlobalWarpsPerCta + warp;
+  if (blockIdx.x * kGlobalWarpsPerCta >= g.warps) return;
+  int *mine = smem + warp * E;
+  for (int i = lane; i < E; i += 32) mine[i] = 0;
+  __syncwarp();
+  const int P = a.M * a.topk;
+  if (gw < g.warps) {
+    const int lo = min(P, gw * g.pairs_per_warp), hi = min(P, lo + g.pairs_per_warp);
+    warp_count(a, l, lo, hi, mine, lane);
+    __syncwarp();
+    int *hist = ws + (size_t)z * slot_stride_ints(g.warps, E) + (size_t)gw * E;
+    for (int i = lane; i < E; i += 32) hist[i] = mine[i];
+  }
+}
+
+__global__ void __launch_bounds__(kScanThreads, 1) align_global_scan_kernel(const AlignArgs a, int *ws,
+                                                                            GlobalLayout g) {
+  extern __shared__ int smem[];
+  const int E = a.num_experts, tid = threadIdx.x;
+  int *cnt = smem;            // [E]
+  int *off = cnt + E;         // [E + 1]
+  int *warp_sums = off + E + 1;
+  const int z = blockIdx.x;
+  const int l = slot_lora(a, z, tid == 0);
+  if (l < 0) return;
+  int *hist = ws + (size_t)z * slot_stride_ints(g.warps, E);
+  if (tid < E) {
+    int run = 0;
+    int w = 0;
+    // four independent loads in flight per step
+    for (; w + 4 <= g.warps; w += 4) {
+      const int t0 = hist[(size_t)(w + 0) * E + tid];
+      const int t1 = hist[(size_t)(w + 1) * E + tid];
+      const int t2 = hist[(size_t)(w + 2) * E + tid];
+      const int t3 = hist[(size_t)(w + 3) * E + tid];
+      hist[(size_t)(w + 0) * E + tid] = run; run += t0;
+      hist[(size_t)(w + 1) * E + tid] = run; run += t1;
+      hist[(size_t)(w + 2) * E + tid] = run; run += t2;
+      hist[(size_t)(w + 3) * E + tid] = run; run += t3;
+    }
+    for (; w < g.warps; ++w) {
+      const int t = hist[(size_t)w * E + tid];
+      hist[(size_t)w * E + tid] = run;
+      run += t;
+    }
+    cnt[tid] = run;
+  }
+  __syncthreads();
+  if (!write_segments(a, l, cnt, off, warp_sums)) {
+    // mark the slot as failed for the scatter kernel
+    if (tid == 0) hist[(size_t)g.warps * E] = -1;
+    return;
+  }
+  if (tid < E) hist[(size_t)g.warps * E + tid] = off[tid];
+}
+
+__global__ void __launch_bounds__(kGlobalThreads) align_global_scatter_kernel(const AlignArgs a, int *ws,
+                                                                              GlobalLayout g) {
+  extern __shared__ int smem[];
+  const int E = a.num_experts;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int z = blockIdx.y;
+  const int l = slot_lora(a, z, false);
+  if (l < 0) return;
+  const int gw = blockIdx.x * kGlobalWarpsPerCta + warp;
+  if (gw >= g.warps) return;
+  const int *slot = ws + (size_t)z * slot_stride_ints(g.warps, E);
+  const int *seg_off = slot + (size_t)g.warps * E;
+  if (__ldg(seg_off) < 0) return;  // capacity failure reported by the scan kernel
+  int *mine = smem + warp * E;
+  const int *base = slot + (size_t)gw * E;
+  for (int i = lane; i < E; i += 32) mine[i] = base[i] + seg_off[i];
+  __syncwarp();
+  const int P = a.M * a.topk;
+  const int lo = min(P, gw * g.pairs_per_warp), hi = min(P, lo + g.pairs_per_warp);
+  warp_scatter(a, l, lo, hi, mine, a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded, lane);
+}
+
+int set_smem_limit(const void *fn, size_t bytes) {
+  if (bytes <= 48 * 1024) return 0;
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
+                 cudaSuccess
+             ? 0
+             : MOE_LORA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+bool align_smem_fits(int E) {
+  const size_t bytes = ((size_t)kSmemWarps * E + 2 * (size_t)E + 1 + 32) * sizeof(int);
+  return bytes <= 200 * 1024;
+}
+
+int align_global_pairs_per_warp(int M, int topk) {
+  const long long P = (long long)M * topk;
+  long long per = (P + kMaxGlobalWarpRanges - 1) / kMaxGlobalWarpRanges;
+  per = (per + 31) / 32 * 32;
+  return (int)(per < 32 ? 32 : per);
+}
+
+size_t align_global_workspace_bytes(int M, int topk, int E, int nact) {
+  const long long P = (long long)M * topk;
+  const int per = align_global_pairs_per_warp(M, topk);
+  const long long W = P > 0 ? (P + per - 1) / per : 1;
+  return (size_t)nact * slot_stride_ints((int)W, E) * sizeof(int);
+}
+
+int launch_align_smem(const AlignArgs &a, cudaStream_t stream) {
+  const size_t bytes = ((size_t)kSmemWarps * a.num_experts + 2 * (size_t)a.num_experts + 1 + 32) *
+                       sizeof(int);
+  if (int st = set_smem_limit((const void *)align_smem_kernel, bytes)) return st;
+  align_smem_kernel<<<a.num_active_loras, kSmemThreads, bytes, stream>>>(a);
+  return cudaGetLastError() == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
+}
+
+int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream) {
+  const long long P = (long long)a.M * a.topk;
+  GlobalLayout g;
+  g.pairs_per_warp = align_global_pairs_per_warp(a.M, a.topk);
+  g.warps = P > 0 ? (int)((P + g.pairs_per_warp - 1) / g.pairs_per_warp) : 1;
+  int *ws = static_cast<int *>(workspace);
+  const int E = a.num_experts;
+  const size_t warp_tab = (size_t)kGlobalWarpsPerCta * E * sizeof(int);
+  const size_t scan_bytes = (2 * (size_t)E + 1 + 32) * sizeof(int);
+  if (int st = set_smem_limit((const void *)align_global_count_kernel, warp_tab)) return st;
+  if (int st = set_smem_limit((const void *)align_global_scatter_kernel, warp_tab)) return st;
+  const dim3 grid((g.warps + kGlobalWarpsPerCta - 1) / kGlobalWarpsPerCta, a.num_active_loras);
+  align_global_count_kernel<<<grid, kGlobalThreads, warp_tab, stream>>>(a, ws, g);
+  align_global_scan_kernel<<<a.num_active_loras, kScanThreads, scan_bytes, stream>>>(a, ws, g);
+  align_global_scatter_kernel<<<grid, kGlobalThreads, warp_tab, stream>>>(a, ws, g);
+  return cudaGetLastError() == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
+}
+
+}  // namespace moe_lora

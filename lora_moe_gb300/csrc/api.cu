@@ -1,0 +1,212 @@
+// api.cu -- the C ABI of libmoe_lora.so (declared in include/moe_lora.h):
+// argument validation, workspace sizing and the choice of align variant and
+// fused path.  Every check runs on the host before anything is enqueued.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "moe_lora.h"
+
+namespace moe_lora {
+
+int current_device_info(DeviceInfo *out) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  static bool have[64] = {};
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_LORA_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!have[dev]) {
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return MOE_LORA_ERR_DEVICE;
+    cache[dev].device = dev;
+    cache[dev].sm_count = prop.multiProcessorCount;
+    cache[dev].major = prop.major;
+    cache[dev].minor = prop.minor;
+    cache[dev].max_smem_optin = prop.sharedMemPerBlockOptin;
+    have[dev] = true;
+  }
+  *out = cache[dev];
+  // The kernels are built for sm_103a (tcgen05, TMA, clusters).
+  if (out->major != 10) return MOE_LORA_ERR_DEVICE;
+  return 0;
+}
+
+}  // namespace moe_lora
+
+using namespace moe_lora;
+
+namespace {
+
+constexpr int kMaxExperts = 1024;   // vLLM PR #29257 review: num_experts <= 1024
+constexpr int kMaxRank = 128;       // PR #42290 summary: the one-shot kernel supports rank <= 128
+constexpr int kMaxSlots = 512;
+
+bool valid_block_size(int bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+long long capacity_tokens(int M, int topk, int E, int bs) {
+  return (long long)M * topk + (long long)E * (bs - 1);
+}
+
+// Shared checks of the sizes both entry points take.
+int check_common(int M, int topk, int E, int max_loras, int nact, int bs, int max_ntp, int max_blocks) {
+  if (M < 0 || topk < 1 || E < 1 || max_loras < 1 || nact < 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (E > kMaxExperts || topk > E) return MOE_LORA_ERR_UNSUPPORTED;
+  if (!valid_block_size(bs)) return MOE_LORA_ERR_UNSUPPORTED;
+  if (nact > max_loras) return MOE_LORA_ERR_INVALID_ARG;
+  if (nact > kMaxSlots) return MOE_LORA_ERR_UNSUPPORTED;
+  const long long cap = capacity_tokens(M, topk, E, bs);
+  if (cap > INT32_MAX / 2) return MOE_LORA_ERR_UNSUPPORTED;
+  if (max_ntp < cap || (long long)max_blocks * bs < cap) return MOE_LORA_ERR_INVALID_ARG;
+  if ((long long)max_loras * max_ntp > INT32_MAX || (long long)max_loras * max_blocks > INT32_MAX)
+    return MOE_LORA_ERR_UNSUPPORTED;
+  return 0;
+}
+
+// The shared-memory variant runs one CTA per active slot; the global variant
+// spreads each slot's pairs over many CTAs.  AUTO takes the global variant for
+// large expert counts (vLLM PR #29257, Purpose) and for long pair lists.
+int resolve_align_variant(int M, int topk, int E, int variant) {
+  if (variant == MOE_LORA_ALIGN_SMEM || variant == MOE_LORA_ALIGN_GLOBAL) return variant;
+  if (!align_smem_fits(E)) return MOE_LORA_ALIGN_GLOBAL;
+  if (E >= 256 || (long long)M * topk >= 16384) return MOE_LORA_ALIGN_GLOBAL;
+  return MOE_LORA_ALIGN_SMEM;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_lora_version(void) { return 100; }
+
+const char *moe_lora_status_string(int status) {
+  switch (status) {
+    case MOE_LORA_OK: return "ok";
+    case MOE_LORA_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_LORA_ERR_UNSUPPORTED: return "unsupported size or option";
+    case MOE_LORA_ERR_MISALIGNED: return "pointer or row not 16-byte aligned";
+    case MOE_LORA_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_LORA_ERR_LAUNCH: return "CUDA launch failed";
+    case MOE_LORA_ERR_DEVICE: return "no usable sm_100-family device";
+    default: return "unknown status";
+  }
+}
+
+int moe_lora_max_num_tokens_padded(int M, int topk, int num_experts, int block_size) {
+  if (M < 0 || topk < 1 || num_experts < 1 || block_size < 1) return -1;
+  const long long cap = capacity_tokens(M, topk, num_experts, block_size);
+  return cap > INT32_MAX ? -1 : (int)cap;
+}
+
+int moe_lora_max_num_m_blocks(int M, int topk, int num_experts, int block_size) {
+  const int cap = moe_lora_max_num_tokens_padded(M, topk, num_experts, block_size);
+  if (cap < 0) return -1;
+  return (cap + block_size - 1) / block_size;
+}
+
+size_t moe_lora_align_workspace_bytes(int M, int topk, int num_experts, int num_active_loras, int block_size,
+                                      int variant) {
+  if (M < 0 || topk < 1 || num_experts < 1 || num_experts > kMaxExperts || num_active_loras < 0 ||
+      !valid_block_size(block_size))
+    return 0;
+  if (resolve_align_variant(M, topk, num_experts, variant) != MOE_LORA_ALIGN_GLOBAL) return 0;
+  return align_global_workspace_bytes(M, topk, num_experts, num_active_loras);
+}
+
+int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                   const int32_t *adapter_enabled, int M, int topk, int num_experts, int max_loras,
+                   int num_active_loras, int block_size, int32_t *sorted_token_ids, int32_t *expert_ids,
+                   int32_t *num_tokens_post_padded, int max_num_tokens_padded, int max_num_m_blocks,
+                   void *workspace, size_t workspace_bytes, int variant, int32_t *err_flag, void *stream) {
+  if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
+                            max_num_m_blocks))
+    return st;
+  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_GLOBAL) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_active_loras == 0) return MOE_LORA_OK;
+  if (!lora_ids || !sorted_token_ids || !expert_ids || !num_tokens_post_padded) return MOE_LORA_ERR_INVALID_ARG;
+  if (M > 0 && (!topk_ids || !token_lora_mapping)) return MOE_LORA_ERR_INVALID_ARG;
+  const int v = resolve_align_variant(M, topk, num_experts, variant);
+  if (v == MOE_LORA_ALIGN_SMEM && !align_smem_fits(num_experts)) return MOE_LORA_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if (int st = current_device_info(&dev)) return st;
+  AlignArgs a;
+  a.topk_ids = topk_ids;
+  a.token_lora_mapping = token_lora_mapping;
+  a.lora_ids = lora_ids;
+  a.adapter_enabled = adapter_enabled;
+  a.sorted_token_ids = sorted_token_ids;
+  a.expert_ids = expert_ids;
+  a.num_tokens_post_padded = num_tokens_post_padded;
+  a.err = err_flag;
+  a.M = M;
+  a.topk = topk;
+  a.num_experts = num_experts;
+  a.max_loras = max_loras;
+  a.num_active_loras = num_active_loras;
+  a.block_size = block_size;
+  a.max_num_tokens_padded = max_num_tokens_padded;
+  a.max_num_m_blocks = max_num_m_blocks;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (v == MOE_LORA_ALIGN_SMEM) return launch_align_smem(a, s);
+  const size_t need = align_global_workspace_bytes(M, topk, num_experts, num_active_loras);
+  if (!workspace || workspace_bytes < need) return MOE_LORA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MOE_LORA_ERR_MISALIGNED;
+  return launch_align_global(a, workspace, s);
+}
+
+int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a, const moe_lora_bf16 *lora_b,
+                                 moe_lora_bf16 *y, const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                                 const int32_t *num_tokens_post_padded, const int32_t *lora_ids,
+                                 const int32_t *adapter_enabled, int M, int topk, int num_experts, int K, int N,
+                                 int rank, int max_loras, int num_active_loras, int block_size,
+                                 int max_num_tokens_padded, int max_num_m_blocks, int add_inputs, int path,
+                                 int32_t *err_flag, void *stream) {
+  if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
+                            max_num_m_blocks))
+    return st;
+  if (K < 8 || N < 8 || rank < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (rank > kMaxRank || rank % 4 != 0) return MOE_LORA_ERR_UNSUPPORTED;
+  if (K % 8 != 0 || N % 8 != 0) return MOE_LORA_ERR_MISALIGNED;
+  if (path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_TCGEN05) return MOE_LORA_ERR_INVALID_ARG;
+  if (path == MOE_LORA_PATH_TCGEN05 && rank % 8 != 0) return MOE_LORA_ERR_UNSUPPORTED;
+  if ((long long)M * K > INT32_MAX * 8LL || (long long)M * topk * N > INT32_MAX * 8LL)
+    return MOE_LORA_ERR_UNSUPPORTED;
+  if (num_active_loras == 0 || M == 0) return MOE_LORA_OK;
+  if (!x || !lora_a || !lora_b || !y || !sorted_token_ids || !expert_ids || !num_tokens_post_padded || !lora_ids)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(lora_a) || !aligned16(lora_b) || !aligned16(y)) return MOE_LORA_ERR_MISALIGNED;
+  FusedArgs f;
+  f.x = x;
+  f.lora_a = lora_a;
+  f.lora_b = lora_b;
+  f.y = y;
+  f.sorted_token_ids = sorted_token_ids;
+  f.expert_ids = expert_ids;
+  f.num_tokens_post_padded = num_tokens_post_padded;
+  f.lora_ids = lora_ids;
+  f.adapter_enabled = adapter_enabled;
+  f.err = err_flag;
+  f.M = M;
+  f.topk = topk;
+  f.num_experts = num_experts;
+  f.K = K;
+  f.N = N;
+  f.rank = rank;
+  f.max_loras = max_loras;
+  f.num_active_loras = num_active_loras;
+  f.block_size = block_size;
+  f.max_num_tokens_padded = max_num_tokens_padded;
+  f.max_num_m_blocks = max_num_m_blocks;
+  f.add_inputs = add_inputs ? 1 : 0;
+  int use = path;
+  if (use == MOE_LORA_PATH_AUTO)
+    use = ((long long)M * topk >= 1024 && rank % 8 == 0) ? MOE_LORA_PATH_TCGEN05 : MOE_LORA_PATH_CUDA_CORE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  return use == MOE_LORA_PATH_TCGEN05 ? launch_fused_tcgen05(f, s) : launch_fused_cuda_core(f, s);
+}
+
+}  // extern "C"

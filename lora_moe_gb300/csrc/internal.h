@@ -1,0 +1,73 @@
+// internal.h -- argument blocks and launchers shared between the C-ABI layer
+// (api.cu) and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace moe_lora {
+
+// Align outputs and inputs, as validated by the C-ABI layer.
+struct AlignArgs {
+  const int32_t *topk_ids;
+  const int32_t *token_lora_mapping;
+  const int32_t *lora_ids;
+  const int32_t *adapter_enabled;  // may be null
+  int32_t *sorted_token_ids;
+  int32_t *expert_ids;
+  int32_t *num_tokens_post_padded;
+  int32_t *err;                    // may be null
+  int M, topk, num_experts, max_loras, num_active_loras, block_size;
+  int max_num_tokens_padded, max_num_m_blocks;
+};
+
+// Fused-stage inputs, as validated by the C-ABI layer.
+struct FusedArgs {
+  const uint16_t *x;       // bf16 [M, K]
+  const uint16_t *lora_a;  // bf16 [L, E, r, K]
+  const uint16_t *lora_b;  // bf16 [L, E, N, r]
+  uint16_t *y;             // bf16 [M, topk, N]
+  const int32_t *sorted_token_ids;
+  const int32_t *expert_ids;
+  const int32_t *num_tokens_post_padded;
+  const int32_t *lora_ids;
+  const int32_t *adapter_enabled;  // may be null
+  int32_t *err;                    // may be null
+  int M, topk, num_experts, K, N, rank, max_loras, num_active_loras, block_size;
+  int max_num_tokens_padded, max_num_m_blocks;
+  int add_inputs;
+};
+
+// Upper bound on the number of blocks all active slots can produce together:
+// every pair belongs to at most one slot, so the blocks are at most
+// floor(M*topk / bs) full ones plus one partly filled block per non-empty
+// (slot, expert) segment.
+inline long long fused_block_bound(int M, int topk, int E, int nact, int bs) {
+  const long long pairs = (long long)M * topk;
+  const long long segs = (long long)nact * E < pairs ? (long long)nact * E : pairs;
+  return pairs / bs + segs;
+}
+
+// Pairs per warp in the global align variant, and its workspace layout:
+// per slot, a [warps][E] table of per-warp expert counts followed by [E]
+// segment offsets.
+int align_global_pairs_per_warp(int M, int topk);
+size_t align_global_workspace_bytes(int M, int topk, int E, int nact);
+bool align_smem_fits(int E);
+
+int launch_align_smem(const AlignArgs &a, cudaStream_t stream);
+int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream);
+int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream);
+int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream);
+
+// Device properties of the current device, cached per device.
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int major, minor;
+  size_t max_smem_optin;
+};
+int current_device_info(DeviceInfo *out);
+
+}  // namespace moe_lora

@@ -1,0 +1,190 @@
+"""GPU parity of the fused shrink+expand against the CPU oracle.
+
+Every output element must satisfy |gpu - ref| <= 1e-2 + 1e-2 |ref| against the
+oracle's unrounded fp64 value; pairs the path does not cover must be left
+bit-identical.  Both paths (CUDA cores, tcgen05) are forced where the shapes
+allow, on the five workloads, on random shapes with ragged K and N tails, on
+exact-integer inputs (bit-exact) and with NaN-poisoned inactive slots."""
+import numpy as np
+import pytest
+
+import oracle
+from lora_moe_gb300 import binding as B
+from lora_moe_gb300 import inputs as gen
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def run_and_compare_full(inp, path, add_inputs=True, adapter_enabled=None, variant=B.ALIGN_AUTO):
+    from helpers import DeviceInputs, gpu_step, host_bf16_bits, check_close, covered
+    d = DeviceInputs(inp)
+    y, err = gpu_step(d, add_inputs=add_inputs, path=path, variant=variant, adapter_enabled=adapter_enabled)
+    assert err == 0, err
+    got = host_bf16_bits(y).reshape(inp.y_in.shape)
+    ref = oracle.fused(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
+                       inp.lora_ids, add_inputs=add_inputs, adapter_enabled=adapter_enabled)
+    cov = covered(inp, adapter_enabled)
+    assert np.array_equal(got[~cov], inp.y_in[~cov]), "uncovered pairs were modified"
+    return check_close(got, ref, "%s path=%d" % (inp.w.name, path))
+
+
+@pytest.mark.parametrize("add_inputs", [True, False])
+@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05, B.PATH_AUTO])
+@pytest.mark.parametrize("name", ["tiny", "decode_qwen3_w13", "decode_gptoss_w2"])
+def test_fused_small_workloads_full(name, path, add_inputs):
+    inp = gen.make_inputs(gen.WORKLOADS[name])
+    run_and_compare_full(inp, path, add_inputs)
+
+
+def small_workload(seed, **kw):
+    rng = np.random.default_rng(seed)
+    base = dict(name="rand%d" % seed, M=int(rng.integers(1, 200)), K=8 * int(rng.integers(1, 120)),
+                N=8 * int(rng.integers(1, 150)), E=int(rng.integers(1, 40)), topk=1, max_loras=int(rng.integers(1, 5)),
+                num_active_loras=1, rank=8 * int(rng.integers(1, 17)), block_size=int(rng.choice([16, 32, 64, 128])),
+                mapping="uniform_with_none", experts="uniform", seed=seed)
+    base["topk"] = int(rng.integers(1, min(base["E"], 8) + 1))
+    base["num_active_loras"] = int(rng.integers(1, base["max_loras"] + 1))
+    base.update(kw)
+    return gen.Workload(**base)
+
+
+@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("seed", range(12))
+def test_fused_random_shapes(seed, path):
+    """Ragged K (not a multiple of the 64-wide K tile) and N (not a multiple of
+    the 128-wide N tile), every block size, ranks 8..128."""
+    inp = gen.make_inputs(small_workload(seed))
+    run_and_compare_full(inp, path, add_inputs=bool(seed % 2))
+
+
+@pytest.mark.parametrize("rank", [4, 12, 20])
+def test_fused_small_ranks_cuda_core(rank):
+    inp = gen.make_inputs(small_workload(77, rank=rank, K=136, N=264))
+    run_and_compare_full(inp, B.PATH_CUDA_CORE)
+
+
+@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("rank", [8, 16, 64, 128])
+def test_fused_ranks(rank, path):
+    inp = gen.make_inputs(small_workload(5, rank=rank, M=96, K=520, N=392, E=6, topk=2, block_size=32))
+    run_and_compare_full(inp, path)
+
+
+@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("rank,nnz", [(8, 16), (16, 8), (64, 2), (128, 1)])
+def test_fused_exact_integer_case(path, rank, nnz):
+    """x, B in {-1, 0, 1}; each row of A has nnz entries in {-1, 1}; y_in in
+    [-4, 4].  Then |t| <= nnz and |ref| <= rank * nnz + 4 <= 260 with every
+    partial sum an integer, exact in fp32 and in bf16 up to 256 -- the GPU must
+    equal the oracle bit for bit.  K = 264 spans five 64-wide K tiles with a
+    ragged tail and N = 392 four 128-wide N tiles (also ragged), so this pins the
+    tensor-core operand layouts, the K accumulation, the cluster reduction and
+    the tails."""
+    from helpers import DeviceInputs, gpu_step, host_bf16_bits
+    w = gen.Workload("int", M=70, K=264, N=392, E=3, topk=2, max_loras=2, num_active_loras=2, rank=rank,
+                     block_size=64, mapping="uniform_with_none", experts="uniform", seed=3)
+    inp = gen.make_inputs(w)
+    rng = np.random.default_rng(8)
+    f2b = gen.f32_to_bf16_bits
+    inp.x = f2b(rng.integers(-1, 2, size=inp.x.shape).astype(np.float32))
+    a = np.zeros(inp.lora_a.shape, np.float32)
+    for idx in np.ndindex(*a.shape[:3]):
+        cols = rng.choice(w.K, nnz, replace=False)
+        a[idx][cols] = rng.choice([-1.0, 1.0], nnz)
+    inp.lora_a = f2b(a)
+    inp.lora_b = f2b(rng.integers(-1, 2, size=inp.lora_b.shape).astype(np.float32))
+    inp.y_in = f2b(rng.integers(-4, 5, size=inp.y_in.shape).astype(np.float32))
+    for add in (True, False):
+        d = DeviceInputs(inp)
+        y, err = gpu_step(d, add_inputs=add, path=path)
+        assert err == 0
+        got = gen.bf16_bits_to_f32(host_bf16_bits(y).reshape(inp.y_in.shape)).astype(np.float64)
+        ref = oracle.fused(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
+                           inp.lora_ids, add_inputs=add)
+        assert np.abs(ref).max() <= 256 or rank * nnz + 4 > 256
+        bad = got != ref
+        assert not bad.any(), "first mismatch at %s: got %r ref %r" % (
+            tuple(np.argwhere(bad)[0]), got[bad][0], ref[bad][0])
+
+
+@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+def test_fused_disabled_adapter_and_poison(path):
+    """Inactive and disabled slots hold NaN in A and B; the output stays finite
+    and their tokens keep y_in."""
+    w = gen.Workload("poison", M=120, K=256, N=256, E=8, topk=2, max_loras=4, num_active_loras=3, rank=16,
+                     block_size=16, mapping="uniform_with_none", experts="uniform", seed=11)
+    inp = gen.make_inputs(w)
+    enabled = np.ones(4, np.int32)
+    enabled[inp.lora_ids[0]] = 0
+    inp.lora_a[inp.lora_ids[0]] = gen.BF16_QNAN
+    inp.lora_b[inp.lora_ids[0]] = gen.BF16_QNAN
+    run_and_compare_full(inp, path, adapter_enabled=enabled)
+
+
+@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+def test_fused_no_covered_pairs(path):
+    from helpers import DeviceInputs, gpu_step, host_bf16_bits
+    w = gen.Workload("none", M=40, K=64, N=128, E=4, topk=2, max_loras=2, num_active_loras=2, rank=8,
+                     block_size=16, mapping="uniform_with_none", experts="uniform", seed=1)
+    inp = gen.make_inputs(w)
+    inp.token_lora_mapping[:] = -1
+    d = DeviceInputs(inp)
+    y, err = gpu_step(d, path=path)
+    assert err == 0 and np.array_equal(host_bf16_bits(y).reshape(inp.y_in.shape), inp.y_in)
+
+
+@pytest.mark.parametrize("variant", [B.ALIGN_SMEM, B.ALIGN_GLOBAL])
+def test_fused_after_either_align_variant(variant):
+    inp = gen.make_inputs(gen.WORKLOADS["decode_gptoss_w2"])
+    run_and_compare_full(inp, B.PATH_AUTO, variant=variant)
+
+
+# ---------------------------------------------------------------- full size
+
+def sampled_compare(inp, path, add_inputs=True, n_pairs=48, n_cols=48, seed=0):
+    """Full-size run; compare sampled covered pairs at sampled columns (and the
+    first / last columns of the N range) with the oracle evaluated one by one;
+    every uncovered pair must be untouched."""
+    import torch
+    from helpers import DeviceInputs, gpu_step, check_close, covered
+    w = inp.w
+    d = DeviceInputs(inp)
+    y, err = gpu_step(d, add_inputs=add_inputs, path=path)
+    assert err == 0, err
+    cov = covered(inp).reshape(-1)
+    rng = np.random.default_rng(seed)
+    cov_idx = np.flatnonzero(cov)
+    pairs = np.sort(rng.choice(cov_idx, min(n_pairs, len(cov_idx)), replace=False)).astype(np.int32)
+    cols = np.unique(np.concatenate([[0, w.N - 1], rng.choice(w.N, n_cols, replace=False)])).astype(np.int32)
+    ref = oracle.fused_sampled(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
+                               inp.lora_ids, pairs, cols, add_inputs=add_inputs)
+    yv = y.view(-1, w.N)
+    got = yv[torch.from_numpy(pairs.astype(np.int64)).cuda()][:, torch.from_numpy(cols.astype(np.int64)).cuda()]
+    got_bits = got.view(torch.int16).cpu().numpy().view(np.uint16)
+    check_close(got_bits, ref, w.name)
+    # every output element finite, uncovered rows bit-identical
+    assert torch.isfinite(y.float()).all()
+    unc = torch.from_numpy(np.flatnonzero(~cov).astype(np.int64)).cuda()
+    y_in = d.y_in.view(-1, w.N)
+    assert torch.equal(yv[unc].view(torch.int16), y_in[unc].view(torch.int16))
+    del d, y
+
+
+@pytest.mark.parametrize("name", ["prefill_mixtral_w13", "large_e_nact1", "large_e_nact4", "large_e_nact8"])
+def test_fused_full_size_sampled(name):
+    inp = gen.make_inputs(gen.WORKLOADS[name])
+    sampled_compare(inp, B.PATH_AUTO)
+
+
+def test_fused_prefill_full_size_cuda_core_sampled():
+    """The CUDA-core path on the prefill shape (it is not the path AUTO picks
+    there, but it must be correct on it)."""
+    inp = gen.make_inputs(gen.WORKLOADS["prefill_mixtral_w13"])
+    sampled_compare(inp, B.PATH_CUDA_CORE, add_inputs=False, n_pairs=24)
