@@ -51,6 +51,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel-seconds", type=float, default=0.3,
                     help="device time spent on each kernel-level timing")
+    ap.add_argument("--profile-steps", type=int, default=0,
+                    help="only run W + this many eager steps (for ncu); prints no JSON line")
+    ap.add_argument("--path", type=int, default=0, help="fused path: 0 auto, 1 CUDA cores, 2 tcgen05")
+    ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0: enough to exceed 3x L2)")
     return ap.parse_args()
 
 
@@ -245,7 +249,7 @@ def run_ours(args, world, rank, local, pg):
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     per_set = (inp.x.nbytes + inp.lora_a.nbytes + inp.lora_b.nbytes + 2 * inp.y_in.nbytes +
                inp.topk_ids.nbytes + inp.token_lora_mapping.nbytes)
-    NB = int(max(2, min(64, -(-3 * l2 // per_set))))
+    NB = args.sets if args.sets > 0 else int(max(2, min(64, -(-3 * l2 // per_set))))
     base = dict(topk_ids=i32(inp.topk_ids), mapping=i32(inp.token_lora_mapping), lora_ids=i32(inp.lora_ids),
                 x=bf16(inp.x), a=bf16(inp.lora_a), b=bf16(inp.lora_b), y=bf16(inp.y_in))
     sets = []
@@ -269,12 +273,20 @@ def run_ours(args, world, rank, local, pg):
         b = s["buf"]
         B.moe_lora_fused_shrink_expand(s["x"], s["a"], s["b"], s["y"], b.sorted_token_ids, b.expert_ids,
                                        b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
-                                       add_inputs=True, err_flag=err, stream=stream)
+                                       add_inputs=True, path=args.path, err_flag=err, stream=stream)
 
     def step(i):
         s = sets[i % NB]
         align(s)
         fused(s)
+
+    if args.profile_steps:
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.profile_steps):
+                step(i)
+        stream.synchronize()
+        assert int(err.item()) == 0, "device error flag %d" % int(err.item())
+        return None
 
     def capture(fn, n):
         g = torch.cuda.CUDAGraph()
@@ -303,12 +315,13 @@ def run_ours(args, world, rank, local, pg):
     barrier(pg, True)
     torch.cuda.synchronize()
     sampler.start()
-    e0.record(stream)
-    for _ in range(args.steps // NB):
-        g_round.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    e1.record(stream)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps // NB):
+            g_round.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
     stream.synchronize()
     torch.cuda.synchronize()
     barrier(pg, True)
@@ -320,21 +333,22 @@ def run_ours(args, world, rank, local, pg):
     # ---------------- kernel-level timing (each kernel alone, same rotation)
     def kernel_time(fn, launches_per_call):
         g = capture(lambda i: fn(sets[i % NB]), NB)
-        g.replay()
-        stream.synchronize()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        g.replay()
-        b.record(stream)
-        stream.synchronize()
-        one = max(1e-6, a.elapsed_time(b))
-        reps = max(1, int(args.kernel_seconds * 1e3 / one))
-        a.record(stream)
-        for _ in range(reps):
+        with torch.cuda.stream(stream):
             g.replay()
-        b.record(stream)
-        stream.synchronize()
+            stream.synchronize()
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            stream.synchronize()
+            one = max(1e-6, a.elapsed_time(b))
+            reps = max(1, int(args.kernel_seconds * 1e3 / one))
+            a.record(stream)
+            for _ in range(reps):
+                g.replay()
+            b.record(stream)
+            stream.synchronize()
         return a.elapsed_time(b) * 1e3 / (reps * NB)   # us per call
 
     fused_us = kernel_time(fused, 1)
@@ -425,6 +439,9 @@ def main():
     import torch
     world, rank, local, pg = dist_setup(True)
     res = run_ours(args, world, rank, local, pg)
+    if res is None:
+        print("profile run done: %d warm-up + %d steps of %s" % (args.warmup, args.profile_steps, w.name))
+        return
     counts = res["counts"]
     us_per_step = res["ms"] * 1e3 / (args.steps * world)
     cpu = None

@@ -5,13 +5,18 @@
 // #42290, "Implementation breakdown" step 1: shrink by lora_a, expand by
 // lora_b, rank dimension kept on chip, add_inputs accumulate/overwrite):
 //     T[p][j] = sum_k x[m_p][k] * A[l][e][j][k]       p < block_size, j < r
-//     y[f_p][n] = bf16((add ? y[f_p][n] : 0) + sum_j B[l][e][n][j] * bf16(T[p][j]))
+//     y[f_p][n] = bf16((add ? y[f_p][n] : 0) + sum_j B[l][e][n][j] * T[p][j])
 //
 // One work item is one (slot, block) of the align output.  A thread-block
 // cluster of C CTAs shares it: CTA c runs the shrink over K-slice c, the C
 // partial T's (fp32, block_size x r) are reduce-scattered through distributed
-// shared memory, every CTA receives the full bf16 T, and CTA c then produces
-// the N-slice c of the block's y rows.  T never reaches global memory.
+// shared memory (summed in rank order, so the result is deterministic), every
+// CTA receives the full T, and CTA c then produces the N-slice c of the block's
+// y rows.  T never reaches global memory.  The expand MMA takes bf16 operands,
+// so T is passed as two bf16 tiles, T_hi = bf16(T) and T_lo = bf16(T - T_hi),
+// and the expand runs over both (the B tile is read twice): the product then
+// carries T to about 16 significant bits instead of 8, which keeps the
+// result within the fp32 path's error.
 //
 // Warp roles (320 threads):
 //   warp 0      producer: gathers the block's x rows with 16-byte cp.async into
@@ -44,8 +49,7 @@ constexpr int kEpiThreads = 256;
 constexpr int kMaxSlots = 512;
 constexpr int kTileK = 64;        // shrink K per stage (one 128-byte swizzle row)
 constexpr int kTileN = 128;       // expand output columns per tile (TMEM lanes)
-constexpr int kXTileBytes = 128 * 128;  // 128 rows x 64 bf16
-constexpr int kLag = 2;           // x-gather stages in flight before a stage is released
+constexpr int kMmaRows = 128;     // M of every tcgen05.mma here
 
 struct TcCfg {
   int C;
@@ -54,9 +58,11 @@ struct TcCfg {
   int s_sh, s_ex;     // pipeline depth of shrink / expand stages
   int tmem_cols;
   // byte offsets from the 1024-aligned smem base
-  int off_sh, sh_stage_bytes, at_offset;   // shrink stage: x tile, then A tile at +at_offset
+  int off_sh, sh_stage_bytes, at_offset;   // shrink stage: x tile (block_size rows), then A tile
+  int lag;            // x-gather stages in flight before a stage is released (< s_sh)
   int off_ex, ex_stage_bytes, yt_offset;   // expand stage: B tile, then y tile at +yt_offset
-  int off_t;          // T tile (bf16, swizzled, natoms x bs rows x 128 B)
+  int off_t;          // T_hi then T_lo tiles (bf16, swizzled, natoms x bs rows x 128 B each)
+  int t_bytes;        // bytes of one T tile
   int tp_pitch;       // floats per row of the fp32 partial T (aliases the shrink stages)
   int off_meta;
   int smem_bytes;     // including alignment slack
@@ -204,19 +210,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           cp_async_16(xt + pr * 128 + ((ch ^ (pr & 7)) << 4), src, ok ? 16u : 0u);
         }
         cp_async_commit();
-        if (issued >= kLag) {
-          cp_async_wait_group<kLag>();
+        if (issued >= cfg.lag) {
+          if (cfg.lag == 1) cp_async_wait_group<1>(); else cp_async_wait_group<2>();
           fence_proxy_async_cta();
-          mbar_arrive(&meta.full_sh[(sh_iter - kLag) % cfg.s_sh]);
+          mbar_arrive(&meta.full_sh[(sh_iter - cfg.lag) % cfg.s_sh]);
         }
       }
       cp_async_wait_group<0>();
       fence_proxy_async_cta();
-      const int tail = issued < kLag ? issued : kLag;
+      const int tail = issued < cfg.lag ? issued : cfg.lag;
       for (int i = tail; i > 0; --i) mbar_arrive(&meta.full_sh[(sh_iter - i) % cfg.s_sh]);
     } else if (warp == 1) {
       if (lane == 0) {
-        const uint32_t idesc = make_idesc_bf16(128, r_pad);
+        const uint32_t idesc = make_idesc_bf16(kMmaRows, r_pad);
         uint32_t first = 1;
         for (int kt = kt0; kt < kt1; ++kt) {
           const int s = sh_iter % cfg.s_sh;
@@ -287,12 +293,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool valid = meta.epi_f[pr] >= 0;
         if (!valid || j >= r) s0 = 0.f;
         if (!valid || j + 1 >= r) s1 = 0.f;
-        const uint32_t packed = (uint32_t)float_to_bf16_bits(s0) | ((uint32_t)float_to_bf16_bits(s1) << 16);
+        const uint16_t h0 = float_to_bf16_bits(s0), h1 = float_to_bf16_bits(s1);
+        const uint16_t l0 = float_to_bf16_bits(s0 - bf16_bits_to_float(h0));
+        const uint16_t l1 = float_to_bf16_bits(s1 - bf16_bits_to_float(h1));
+        const uint32_t hi = (uint32_t)h0 | ((uint32_t)h1 << 16);
+        const uint32_t lo = (uint32_t)l0 | ((uint32_t)l1 << 16);
         const int jj = j & 63;
         const size_t off = (size_t)(j >> 6) * (BS * 128) + (size_t)pr * 128 +
                            ((((jj >> 3) ^ (pr & 7)) << 4)) + (jj & 7) * 2;
-        for (int q = 0; q < C; ++q)
-          *reinterpret_cast<uint32_t *>(cluster.map_shared_rank(t_tile + off, q)) = packed;
+        for (int q = 0; q < C; ++q) {
+          *reinterpret_cast<uint32_t *>(cluster.map_shared_rank(t_tile + off, q)) = hi;
+          *reinterpret_cast<uint32_t *>(cluster.map_shared_rank(t_tile + cfg.t_bytes + off, q)) = lo;
+        }
       }
       fence_proxy_async_cluster();
     }
@@ -333,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (warp == 1) {
       if (lane == 0) {
-        const uint32_t idesc = make_idesc_bf16(128, BS);
+        const uint32_t idesc = make_idesc_bf16(kMmaRows, BS);
         const uint32_t ta = smem_addr(t_tile);
         fence_proxy_async_cta();
         for (int nt = nt0; nt < nt1; ++nt) {
@@ -343,10 +355,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (acc_iter >= 2) mbar_wait(&meta.tempty[a], ((acc_iter >> 1) - 1) & 1, abort, p.err);
           tc_fence_after();
           const uint32_t ba = smem_addr(ex_base + (size_t)s * cfg.ex_stage_bytes);
-          for (int ks = 0; ks < r_pad / 16; ++ks) {
-            const uint32_t atom = ks >> 2, within = (ks & 3) * 32;
-            tc_mma_bf16(tmem + a * BS, make_sdesc_sw128(ba + atom * (kTileN * 128) + within),
-                        make_sdesc_sw128(ta + atom * (BS * 128) + within), idesc, ks > 0 ? 1u : 0u);
+          for (int part = 0; part < 2; ++part) {          // T_hi, then T_lo
+            const uint32_t tp = ta + part * cfg.t_bytes;
+            for (int ks = 0; ks < r_pad / 16; ++ks) {
+              const uint32_t atom = ks >> 2, within = (ks & 3) * 32;
+              tc_mma_bf16(tmem + a * BS, make_sdesc_sw128(ba + atom * (kTileN * 128) + within),
+                          make_sdesc_sw128(tp + atom * (BS * 128) + within), idesc,
+                          (part | ks) ? 1u : 0u);
+            }
           }
           tc_commit(&meta.tfull[a]);
           tc_commit(&meta.empty_ex[s]);
@@ -467,41 +483,47 @@ int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, TcCfg *cfg) {
   if (C > BS) C = BS;
   if (C < 1) C = 1;
   cfg->C = C;
-  cfg->tp_pitch = cfg->r_pad + 4;
+  // Shrink stage: the x tile holds block_size rows; the M=128 MMA also reads
+  // the 128 - block_size rows after them (the A tile, or the next region),
+  // whose products land in accumulator rows nobody reads.
   const int at_bytes = cfg->r_pad * 128;
-  cfg->at_offset = kXTileBytes;
-  cfg->sh_stage_bytes = kXTileBytes + at_bytes;
+  cfg->at_offset = BS * 128;
+  cfg->sh_stage_bytes = (BS * 128 + at_bytes + 1023) / 1024 * 1024;
   cfg->yt_offset = cfg->natoms * kTileN * 128;
   cfg->ex_stage_bytes = (cfg->yt_offset + BS * kTileN * 2 + 1023) / 1024 * 1024;
-  const int t_bytes = cfg->natoms * BS * 128;
-  const int tpart_bytes = BS * cfg->tp_pitch * 4;
+  cfg->t_bytes = cfg->natoms * BS * 128;
   const int meta_bytes = (int)((sizeof(TcMeta) + 1023) / 1024 * 1024);
   const int budget = (int)dev.max_smem_optin - 1024;  // alignment slack
-  // s_sh > kLag: a stage is released kLag iterations after it is issued.
-  for (int s_sh = 4; s_sh > kLag; --s_sh) {
-    for (int s_ex = 4; s_ex >= 2; --s_ex) {
+  static const int plans[][2] = {{4, 4}, {3, 4}, {3, 3}, {4, 2}, {3, 2}, {2, 2}, {3, 1}, {2, 1}};
+  for (int pitch_pad = 4; pitch_pad >= 0; pitch_pad -= 4) {
+    cfg->tp_pitch = cfg->r_pad + pitch_pad;   // +4 floats staggers rows across banks
+    const int tpart_bytes = BS * cfg->tp_pitch * 4;
+    for (const auto &pl : plans) {
+      const int s_sh = pl[0], s_ex = pl[1];
       int sh_region = s_sh * cfg->sh_stage_bytes;
       if (sh_region < tpart_bytes) sh_region = (tpart_bytes + 1023) / 1024 * 1024;
-      const int total = sh_region + s_ex * cfg->ex_stage_bytes + t_bytes + meta_bytes;
-      if (total <= budget) {
-        cfg->s_sh = s_sh;
-        cfg->s_ex = s_ex;
-        cfg->off_sh = 0;
-        cfg->off_ex = sh_region;
-        cfg->off_t = sh_region + s_ex * cfg->ex_stage_bytes;
-        cfg->off_meta = cfg->off_t + t_bytes;
-        cfg->smem_bytes = total + 1024;
-        int cols = 32;
-        while (cols < 2 * BS + cfg->r_pad) cols <<= 1;
-        cfg->tmem_cols = cols;
-        // CTAs that share an SM share its 512 TMEM columns: ask for enough shared
-        // memory that they never need more (an allocation that cannot be met
-        // would wait for a CTA that may itself wait on this one's cluster).
-        const int per_sm = 228 * 1024;
-        while ((per_sm / (cfg->smem_bytes + 1024)) * cols > 512) cfg->smem_bytes += 4096;
-        if (cfg->smem_bytes > (int)dev.max_smem_optin) return MOE_LORA_ERR_UNSUPPORTED;
-        return 0;
-      }
+      // (the last x tile's over-read, at most (128 - block_size) rows, stays
+      // inside the expand stages that follow the shrink region)
+      const int total = sh_region + s_ex * cfg->ex_stage_bytes + 2 * cfg->t_bytes + meta_bytes;
+      if (total > budget) continue;
+      cfg->s_sh = s_sh;
+      cfg->s_ex = s_ex;
+      cfg->lag = s_sh - 1 < 2 ? s_sh - 1 : 2;
+      cfg->off_sh = 0;
+      cfg->off_ex = sh_region;
+      cfg->off_t = sh_region + s_ex * cfg->ex_stage_bytes;
+      cfg->off_meta = cfg->off_t + 2 * cfg->t_bytes;
+      cfg->smem_bytes = total + 1024;
+      int cols = 32;
+      while (cols < 2 * BS + cfg->r_pad) cols <<= 1;
+      cfg->tmem_cols = cols;
+      // CTAs that share an SM share its 512 TMEM columns: ask for enough shared
+      // memory that they never need more (an allocation that cannot be met
+      // would wait for a CTA that may itself wait on this one's cluster).
+      const int per_sm = 228 * 1024;
+      while ((per_sm / (cfg->smem_bytes + 1024)) * cols > 512) cfg->smem_bytes += 4096;
+      if (cfg->smem_bytes > (int)dev.max_smem_optin) return MOE_LORA_ERR_UNSUPPORTED;
+      return 0;
     }
   }
   return MOE_LORA_ERR_UNSUPPORTED;

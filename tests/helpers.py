@@ -63,7 +63,7 @@ def assert_align_equal(topk_ids, mapping, lora_ids, E, L, bs, variant=B.ALIGN_AU
 
 
 class DeviceInputs:
-    def __init__(self, inp: gen.Inputs):
+    def __init__(self, inp: gen.Inputs, variant=B.ALIGN_AUTO):
         w = inp.w
         self.w = w
         self.topk_ids = dev_i32(inp.topk_ids)
@@ -73,7 +73,8 @@ class DeviceInputs:
         self.a = dev_bf16(inp.lora_a)
         self.b = dev_bf16(inp.lora_b)
         self.y_in = dev_bf16(inp.y_in)
-        self.buf = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size)
+        self.buf = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size,
+                                  variant=variant)
 
 
 def gpu_step(d: DeviceInputs, add_inputs=True, path=B.PATH_AUTO, variant=B.ALIGN_AUTO, adapter_enabled=None,

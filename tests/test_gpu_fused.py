@@ -24,7 +24,7 @@ def _cuda():
 
 def run_and_compare_full(inp, path, add_inputs=True, adapter_enabled=None, variant=B.ALIGN_AUTO):
     from helpers import DeviceInputs, gpu_step, host_bf16_bits, check_close, covered
-    d = DeviceInputs(inp)
+    d = DeviceInputs(inp, variant)
     y, err = gpu_step(d, add_inputs=add_inputs, path=path, variant=variant, adapter_enabled=adapter_enabled)
     assert err == 0, err
     got = host_bf16_bits(y).reshape(inp.y_in.shape)
