@@ -23,6 +23,8 @@
 //                           scatter) replace the CTA-wide barriers.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "device_utils.cuh"
 #include "internal.h"
 
@@ -163,32 +165,85 @@ __device__ bool write_segments(const AlignArgs &a, int l, const int *cnt, int *o
 
 // ----------------------------------------------------- shared-memory variant
 
+constexpr int kCache = 8;   // warp-widths of expert ids a lane keeps between the two walks
+
+// The two walks of one warp over [lo, hi) with the experts kept in registers
+// between them (hi - lo <= kCache * 32); `tab` is this warp's counter row.
+__device__ __forceinline__ void warp_count_cached(const AlignArgs &a, int l, int lo, int hi, int *tab, int lane,
+                                                  int (&ec)[kCache]) {
+#pragma unroll
+  for (int it = 0; it < kCache; ++it) {
+    const int base = lo + it * 32;
+    ec[it] = -1;
+    if (base < hi) {
+      const int f = base + lane;
+      const int e = (f < hi) ? pair_expert(a, f, l, true) : -1;
+      ec[it] = e;
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(peers) - 1) tab[e] += __popc(peers);
+    }
+  }
+}
+
+__device__ __forceinline__ void warp_scatter_cached(int lo, int hi, int *tab, int32_t *sorted, int lane,
+                                                    const int (&ec)[kCache]) {
+  const unsigned lower = (1u << lane) - 1u;
+#pragma unroll
+  for (int it = 0; it < kCache; ++it) {
+    const int base = lo + it * 32;
+    if (base < hi) {
+      const int e = ec[it];
+      const unsigned peers = __match_any_sync(0xffffffffu, e);
+      const int pos = (e >= 0) ? tab[e] + __popc(peers & lower) : 0;
+      __syncwarp();
+      if (e >= 0) {
+        sorted[pos] = base + lane;
+        if (lane == __ffs(peers) - 1) tab[e] += __popc(peers);
+      }
+      __syncwarp();
+    }
+  }
+}
+
+// One CTA of 1024 threads per active slot.  The pairs are split over the
+// first W warps (W = min(32, ceil(P / 32))), each a contiguous range; the
+// per-warp counters form a W x E table in shared memory.
 __global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const AlignArgs a) {
   extern __shared__ int smem[];
   const int E = a.num_experts;
-  int *tab = smem;                          // [kSmemWarps][E] per-warp counters / cursors
-  int *cnt = tab + kSmemWarps * E;          // [E]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = a.M * a.topk;
+  const int W = max(1, min(kSmemWarps, (P + 31) / 32));
+  int *tab = smem;                          // [W][E] per-warp counters, then cursors
+  int *cnt = tab + W * E;                   // [E]
   int *off = cnt + E;                       // [E + 1]
   int *warp_sums = off + E + 1;             // [32]
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  // The fused kernel may be launched as this grid's programmatic dependent; it
+  // waits for this grid's completion before it reads any output.
+  asm volatile("griddepcontrol.launch_dependents;");
 
   const int l = slot_lora(a, blockIdx.x, tid == 0);
   if (l < 0) return;
 
-  for (int i = tid; i < kSmemWarps * E; i += kSmemThreads) tab[i] = 0;
+  for (int i = tid; i < W * E; i += kSmemThreads) tab[i] = 0;
   __syncthreads();
 
-  const int P = a.M * a.topk;
-  const int per_warp = ((P + kSmemWarps - 1) / kSmemWarps + 31) / 32 * 32;
-  const int lo = min(P, warp * per_warp), hi = min(P, lo + per_warp);
-  int *mine = tab + warp * E;
-  warp_count(a, l, lo, hi, mine, lane);
+  const int per_warp = ((P + W - 1) / W + 31) / 32 * 32;
+  const int lo = min(P, warp * per_warp), hi = warp < W ? min(P, lo + per_warp) : lo;
+  const bool cached = per_warp <= kCache * 32;
+  int *mine = tab + (warp < W ? warp : 0) * E;
+  int ec[kCache];
+  if (warp < W) {
+    if (cached) warp_count_cached(a, l, lo, hi, mine, lane, ec);
+    else warp_count(a, l, lo, hi, mine, lane);
+  }
   __syncthreads();
 
   // Column scan: each warp's starting position relative to its segment.
   if (tid < E) {
     int run = 0;
-    for (int w = 0; w < kSmemWarps; ++w) {
+    for (int w = 0; w < W; ++w) {
       const int t = tab[w * E + tid];
       tab[w * E + tid] = run;
       run += t;
@@ -198,11 +253,14 @@ __global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const Align
   __syncthreads();
   if (!write_segments(a, l, cnt, off, warp_sums)) return;
   if (tid < E)
-    for (int w = 0; w < kSmemWarps; ++w) tab[w * E + tid] += off[tid];
+    for (int w = 0; w < W; ++w) tab[w * E + tid] += off[tid];
   __syncthreads();
 
-  warp_scatter(a, l, lo, hi, mine,
-               a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded, lane);
+  if (warp < W) {
+    int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
+    if (cached) warp_scatter_cached(lo, hi, mine, sorted, lane, ec);
+    else warp_scatter(a, l, lo, hi, mine, sorted, lane);
+  }
 }
 
 // ----------------------------------------------------- global-memory variant
@@ -282,6 +340,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) align_global_scan_kernel(cons
 __global__ void __launch_bounds__(kGlobalThreads) align_global_scatter_kernel(const AlignArgs a, int *ws,
                                                                               GlobalLayout g) {
   extern __shared__ int smem[];
+  asm volatile("griddepcontrol.launch_dependents;");
   const int E = a.num_experts;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int z = blockIdx.y;
@@ -331,8 +390,9 @@ size_t align_global_workspace_bytes(int M, int topk, int E, int nact) {
 }
 
 int launch_align_smem(const AlignArgs &a, cudaStream_t stream) {
-  const size_t bytes = ((size_t)kSmemWarps * a.num_experts + 2 * (size_t)a.num_experts + 1 + 32) *
-                       sizeof(int);
+  const long long P = (long long)a.M * a.topk;
+  const int W = (int)std::max(1LL, std::min<long long>(kSmemWarps, (P + 31) / 32));
+  const size_t bytes = ((size_t)W * a.num_experts + 2 * (size_t)a.num_experts + 1 + 32) * sizeof(int);
   if (int st = set_smem_limit((const void *)align_smem_kernel, bytes)) return st;
   align_smem_kernel<<<a.num_active_loras, kSmemThreads, bytes, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;

@@ -127,6 +127,11 @@ __device__ __forceinline__ void cp_async_16(void *dst, const void *src, uint32_t
                "r"(src_bytes)
                : "memory");
 }
+// Arrive on `bar` (counted as one of its expected arrivals) once every
+// cp.async this thread issued before has completed.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
@@ -146,6 +151,11 @@ __device__ __forceinline__ void fence_proxy_async_cluster() {
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// (the align kernel) has completed and its writes are visible.  A no-op when
+// the kernel was not launched as a dependent.
+__device__ __forceinline__ void wait_for_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ tcgen05
 

@@ -10,19 +10,21 @@
 // rank dimension on chip; its small-batch kernel is the decode specialisation.)
 //
 // At decode sizes a block holds one or two real pairs, so the work is a skinny
-// GEMV bound by reading A[l,e] (r x K) and B[l,e] (N x r).  To spread those
-// bytes over many SMs, each block is processed by a thread-block cluster of C
-// CTAs: CTA c reads the K-slice c of A and of the gathered x rows and forms a
-// partial t; the C partials are summed through distributed shared memory (in
-// rank order, so the result is deterministic); then CTA c produces the N-slice
-// c of y from its slice of B.  Every operand moves global -> shared with 1-D
-// bulk (TMA) copies completing on an mbarrier, all issued before the first
-// wait; the first B slice is fetched while the shrink runs.  Dot products use
-// 16-byte shared-memory vectors and warp-shuffle reductions.  The y rows are
-// written back with bulk stores.  The grid covers only active slots: clusters
-// walk the blocks of all listed slots (vLLM PR #32005, grid sized by
-// num_active_loras rather than max_loras).
+// GEMV bound by reading A[l,e] (r x K) and B[l,e] (N x r) -- and, at a few
+// megabytes per call, by latency.  Design:
+//   * grid (C, num_active_loras, blocks): CTA (c, z, b) serves block b of slot z
+//     (vLLM PR #32005: the LoRA grid dimension is the number of active LoRAs);
+//     blocks past num_tokens_post_padded exit after one dependent load.
+//   * a thread-block cluster of C CTAs shares a block: CTA c streams the
+//     K-slice c of A and of the gathered x rows and the N-slice c of B and y;
+//     the C partial t's are summed through distributed shared memory in rank
+//     order (deterministic).
+//   * every operand is requested at once, before the first wait: A, x and y_in
+//     rows with 16-byte cp.async (load/store unit), the contiguous B slice with
+//     one bulk copy.  Dot products read 16-byte shared-memory vectors and reduce
+//     with warp shuffles; y is written with coalesced stores.
 #include <cooperative_groups.h>
+#include <algorithm>
 #include <cuda_runtime.h>
 
 #include "device_utils.cuh"
@@ -36,23 +38,21 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kPG = 16;          // pairs processed together
+constexpr int kPG = 8;           // pairs processed together
 constexpr int kMaxBlock = 128;   // largest block_size
-constexpr int kMaxSlots = 512;   // largest num_active_loras
+constexpr int kMaxCluster = 16;
 
 struct CcCfg {
-  int C;          // CTAs per block (cluster size)
-  int kc, nc;     // K columns / N rows per chunk (multiples of 8)
-  int a_pitch;    // bytes per staged A row (kc + 8 bf16, a 16-byte skew between rows)
+  int C;               // CTAs per block (cluster size)
+  int kslice, nslice;  // per-CTA K / N slice capacity (multiples of 8)
+  int a_pitch;         // bytes per staged A row (kslice + 8 bf16: rows skewed by 16 B)
   int off_a, off_x, off_b, off_y, off_tp, off_tf;
   int smem_bytes;
 };
 
 struct Meta {
-  uint64_t bar[2];               // 0: A + x loads, 1: B + y loads
-  int slot_l[kMaxSlots];
-  int prefix[kMaxSlots + 1];
-  int pf[kMaxBlock];             // the block's real pairs (flat index), compacted in order
+  uint64_t bar;                  // the B slice's bulk copy
+  int pf[kMaxBlock];             // the block's real pairs (flat index), in order
   int pm[kMaxBlock];             // their token index
   int wcount[kWarps];
   int nv;
@@ -83,6 +83,7 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const uint4 xv) {
   return s;
 }
 
+// RV: elements of B per shared-memory vector (8 when rank % 8 == 0, else 4).
 template <int RV>
 __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedArgs p, const CcCfg cfg) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -100,68 +101,43 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = p.rank, K = p.K, N = p.N, E = p.num_experts, bs = p.block_size;
   const int P = p.M * p.topk;
+  const int z = blockIdx.y;
+
+  // Uniform over the cluster: every CTA of it reads the same values.
+  const int l = __ldg(p.lora_ids + z);
+  if (l < 0 || l >= p.max_loras) {
+    if (c == 0 && tid == 0 && blockIdx.z == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
+    return;
+  }
+  if (p.adapter_enabled && __ldg(p.adapter_enabled + l) == 0) return;
+  wait_for_prior_grid();   // align outputs are read from here on
+  const int nblocks = min(__ldg(p.num_tokens_post_padded + l) / bs, p.max_num_m_blocks);
+  if ((int)blockIdx.z >= nblocks) return;
 
   if (tid == 0) {
-    mbar_init(&meta.bar[0], 1);
-    mbar_init(&meta.bar[1], 1);
+    mbar_init(&meta.bar, 1);
     meta.abort = 0;
     fence_barrier_init();
   }
-  // Blocks per listed slot, and their prefix sum: the work list of the grid.
-  for (int z = tid; z < p.num_active_loras; z += kThreads) {
-    const int l = __ldg(p.lora_ids + z);
-    int nb = 0;
-    if (l < 0 || l >= p.max_loras) {
-      if (c == 0 && blockIdx.y == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
-    } else if (!p.adapter_enabled || __ldg(p.adapter_enabled + l) != 0) {
-      nb = __ldg(p.num_tokens_post_padded + l) / bs;
-      nb = max(0, min(nb, p.max_num_m_blocks));
-    }
-    meta.slot_l[z] = l;
-    meta.prefix[z + 1] = nb;
-  }
   __syncthreads();
-  if (tid == 0) {
-    meta.prefix[0] = 0;
-    for (int z = 0; z < p.num_active_loras; ++z) meta.prefix[z + 1] += meta.prefix[z];
-  }
-  __syncthreads();
-  const int total_blocks = meta.prefix[p.num_active_loras];
+  volatile int *abort = &meta.abort;
+  uint32_t phase = 0;
 
   // This CTA's K- and N-slices, in units of 8 elements.
   const int k8 = K / 8, n8 = N / 8;
   const int k_lo = (c * k8 / C) * 8, k_hi = ((c + 1) * k8 / C) * 8;
   const int n_lo = (c * n8 / C) * 8, n_hi = ((c + 1) * n8 / C) * 8;
-  const int nk_chunks = (k_hi - k_lo + cfg.kc - 1) / cfg.kc;
-  const int nn_chunks = (n_hi - n_lo + cfg.nc - 1) / cfg.nc;
-  uint32_t ph0 = 0, ph1 = 0;
-  volatile int *abort = &meta.abort;
+  const int kn = k_hi - k_lo, nn = n_hi - n_lo;
 
-  for (int item = blockIdx.y; item < total_blocks; item += gridDim.y) {
-    // Locate (slot, block) of this work item.
-    int z = 0;
-    {
-      int lo = 0, hi = p.num_active_loras;  // prefix[lo] <= item < prefix[hi]
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (meta.prefix[mid] <= item) lo = mid; else hi = mid;
-      }
-      z = lo;
-    }
-    const int l = meta.slot_l[z];
-    const int b = item - meta.prefix[z];
+  for (int b = blockIdx.z; b < nblocks; b += gridDim.z) {
     const int e = __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b);
-    if (e < 0 || e >= E) {  // uniform over the cluster: every CTA reads the same entry
-      if (tid == 0 && c == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
-      continue;
-    }
     // Compact the block's real pairs, keeping their order.
     {
-      const int32_t *ids = p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + (size_t)b * bs;
+      const int idx = b * bs + tid;
       int f = -1;
-      if (tid < bs) {
-        f = __ldg(ids + tid);
-        if (f != P && (f < 0 || f > P)) {
+      if (tid < bs && idx < p.max_num_tokens_padded) {
+        f = __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + idx);
+        if (f < 0 || f > P) {
           if (c == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
           f = -1;
         } else if (f == P) {
@@ -172,8 +148,9 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
       if (lane == 0) meta.wcount[warp] = __popc(bal);
       __syncthreads();
       int base = 0, tot = 0;
+#pragma unroll
       for (int w = 0; w < kWarps; ++w) {
-        if (w < warp) base += meta.wcount[w];
+        base += (w < warp) ? meta.wcount[w] : 0;
         tot += meta.wcount[w];
       }
       if (f >= 0) {
@@ -184,49 +161,48 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
       if (tid == 0) meta.nv = tot;
       __syncthreads();
     }
+    if (e < 0 || e >= E) {  // uniform over the cluster
+      if (tid == 0 && c == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
+      continue;
+    }
     const int nv = meta.nv;
     const size_t le = (size_t)l * E + e;
     const uint16_t *A = p.lora_a + le * r * K;
-    const uint16_t *B = p.lora_b + le * N * r;
+    const uint16_t *Bm = p.lora_b + le * N * r;
 
     for (int g0 = 0; g0 < nv; g0 += kPG) {
       const int nvg = min(kPG, nv - g0);
-      // Issue the first B slice (and y rows) now so that they arrive during the shrink.
-      auto issue_expand = [&](int nc0) {
-        const int ncn = min(cfg.nc, n_hi - nc0);
-        if (warp == 0) {
-          const uint32_t bytes = (uint32_t)ncn * r * 2 + (p.add_inputs ? (uint32_t)nvg * ncn * 2 : 0u);
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&meta.bar[1], bytes);
-            bulk_g2s(b_s, B + (size_t)nc0 * r, (uint32_t)ncn * r * 2, &meta.bar[1]);
+      // ---- request every operand of this group at once
+      if (g0 == 0 && tid == 0) {
+        mbar_arrive_expect_tx(&meta.bar, (uint32_t)nn * r * 2);
+        bulk_g2s(b_s, Bm + (size_t)n_lo * r, (uint32_t)nn * r * 2, &meta.bar);
+      }
+      {
+        const int kch = kn / 8, nch = nn / 8;
+        if (g0 == 0)
+          for (int i = tid; i < r * kch; i += kThreads) {
+            const int j = i / kch, ch = i - j * kch;
+            cp_async_16(a_s + (size_t)j * cfg.a_pitch + ch * 16, A + (size_t)j * K + k_lo + ch * 8, 16u);
           }
-          __syncwarp();
-          if (p.add_inputs)
-            for (int q = lane; q < nvg; q += 32)
-              bulk_g2s(y_s + (size_t)q * cfg.nc * 2, p.y + (size_t)meta.pf[g0 + q] * N + nc0,
-                       (uint32_t)ncn * 2, &meta.bar[1]);
+        for (int i = tid; i < nvg * kch; i += kThreads) {
+          const int q = i / kch, ch = i - q * kch;
+          cp_async_16(x_s + (size_t)q * cfg.kslice * 2 + ch * 16,
+                      p.x + (size_t)meta.pm[g0 + q] * K + k_lo + ch * 8, 16u);
         }
-      };
-      issue_expand(n_lo);
-
-      // ---- shrink: partial t over this CTA's K-slice
-      for (int i = tid; i < nvg * r; i += kThreads) tpart[i] = 0.f;
+        if (p.add_inputs)
+          for (int i = tid; i < nvg * nch; i += kThreads) {
+            const int q = i / nch, ch = i - q * nch;
+            cp_async_16(y_s + (size_t)q * cfg.nslice * 2 + ch * 16,
+                        p.y + (size_t)meta.pf[g0 + q] * N + n_lo + ch * 8, 16u);
+          }
+        cp_async_commit();
+      }
+      cp_async_wait_group<0>();
       __syncthreads();
-      for (int kci = 0; kci < nk_chunks; ++kci) {
-        const int kc0 = k_lo + kci * cfg.kc;
-        const int kcn = min(cfg.kc, k_hi - kc0);
-        if (warp == 0) {
-          if (lane == 0) mbar_arrive_expect_tx(&meta.bar[0], (uint32_t)(r + nvg) * kcn * 2);
-          __syncwarp();
-          for (int j = lane; j < r; j += 32)
-            bulk_g2s(a_s + (size_t)j * cfg.a_pitch, A + (size_t)j * K + kc0, (uint32_t)kcn * 2, &meta.bar[0]);
-          for (int q = lane; q < nvg; q += 32)
-            bulk_g2s(x_s + (size_t)q * cfg.kc * 2, p.x + (size_t)meta.pm[g0 + q] * K + kc0,
-                     (uint32_t)kcn * 2, &meta.bar[0]);
-        }
-        mbar_wait(&meta.bar[0], ph0, abort, p.err);
-        ph0 ^= 1;
-        const int nch = kcn / 8;
+
+      // ---- shrink: partial t over this CTA's K-slice; warp w owns rows j = w (mod 8)
+      {
+        const int nch = kn / 8;
         for (int j = warp; j < r; j += kWarps) {
           float acc[kPG];
 #pragma unroll
@@ -237,7 +213,8 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
             unpack8(arow[ch], af);
 #pragma unroll
             for (int q = 0; q < kPG; ++q)
-              if (q < nvg) acc[q] += dot8(af, reinterpret_cast<const uint4 *>(x_s + (size_t)q * cfg.kc * 2)[ch]);
+              if (q < nvg)
+                acc[q] += dot8(af, reinterpret_cast<const uint4 *>(x_s + (size_t)q * cfg.kslice * 2)[ch]);
           }
 #pragma unroll
           for (int q = 0; q < kPG; ++q) {
@@ -245,11 +222,10 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
               float v = acc[q];
 #pragma unroll
               for (int d = 16; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-              if (lane == 0) tpart[q * r + j] += v;
+              if (lane == 0) tpart[q * r + j] = v;
             }
           }
         }
-        __syncthreads();
       }
 
       // ---- sum the C partial t's through distributed shared memory
@@ -261,34 +237,30 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
           for (int q = 0; q < C; ++q) s += cluster.map_shared_rank(tpart, q)[i];
           tfull[i] = s;
         }
-        cluster.sync();
         t = tfull;
       }
+      __syncthreads();
+      if (g0 == 0) mbar_wait(&meta.bar, phase, abort, p.err);
 
-      // ---- expand: y rows of this CTA's N-slice
-      constexpr int kLanesMax = 16;
-      const int vecs = r / RV;                 // vectors per B row
-      int lpr = 1;                             // lanes per B row (power of two)
-      while (lpr < vecs && lpr < kLanesMax) lpr <<= 1;
-      const int rows_per_warp = 32 / lpr;
-      for (int nci = 0; nci < nn_chunks; ++nci) {
-        const int nc0 = n_lo + nci * cfg.nc;
-        const int ncn = min(cfg.nc, n_hi - nc0);
-        if (nci > 0) issue_expand(nc0);
-        mbar_wait(&meta.bar[1], ph1, abort, p.err);
-        ph1 ^= 1;
-        for (int row0 = warp * rows_per_warp; row0 < ncn; row0 += kWarps * rows_per_warp) {
+      // ---- expand: y rows of this CTA's N-slice.  A B row is read by lpr lanes
+      // (one shared-memory vector each); their partial sums meet by shuffles.
+      {
+        const int vecs = r / RV;
+        int lpr = 1;
+        while (lpr < vecs && lpr < 16) lpr <<= 1;
+        const int rows_per_warp = 32 / lpr;
+        for (int row0 = warp * rows_per_warp; row0 < nn; row0 += kWarps * rows_per_warp) {
           const int nl = row0 + lane / lpr;
           const int ch0 = lane % lpr;
           float acc[kPG];
 #pragma unroll
           for (int q = 0; q < kPG; ++q) acc[q] = 0.f;
-          if (nl < ncn) {
+          if (nl < nn) {
             for (int ch = ch0; ch < vecs; ch += lpr) {
               const int j0 = ch * RV;
               if constexpr (RV == 8) {
                 float bf[8];
-                unpack8(reinterpret_cast<const uint4 *>(b_s + ((size_t)nl * r + j0) * 2)[0], bf);
+                unpack8(*reinterpret_cast<const uint4 *>(b_s + ((size_t)nl * r + j0) * 2), bf);
 #pragma unroll
                 for (int q = 0; q < kPG; ++q) {
                   if (q < nvg) {
@@ -300,7 +272,7 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
                 }
               } else {
                 float bf[4];
-                unpack4(reinterpret_cast<const uint2 *>(b_s + ((size_t)nl * r + j0) * 2)[0], bf);
+                unpack4(*reinterpret_cast<const uint2 *>(b_s + ((size_t)nl * r + j0) * 2), bf);
 #pragma unroll
                 for (int q = 0; q < kPG; ++q) {
                   if (q < nvg) {
@@ -316,69 +288,67 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
             if (q < nvg) {
               float v = acc[q];
               for (int d = lpr >> 1; d > 0; d >>= 1) v += __shfl_xor_sync(0xffffffffu, v, d);
-              if (ch0 == 0 && nl < ncn) {
-                uint16_t *dst = reinterpret_cast<uint16_t *>(y_s + (size_t)q * cfg.nc * 2) + nl;
-                const float old = p.add_inputs ? bf16_bits_to_float(*dst) : 0.f;
-                *dst = float_to_bf16_bits(v + old);
+              if (ch0 == 0 && nl < nn) {
+                const float old = p.add_inputs
+                                      ? bf16_bits_to_float(reinterpret_cast<const uint16_t *>(
+                                            y_s + (size_t)q * cfg.nslice * 2)[nl])
+                                      : 0.f;
+                p.y[(size_t)meta.pf[g0 + q] * N + n_lo + nl] = float_to_bf16_bits(v + old);
               }
             }
           }
         }
-        fence_proxy_async_cta();
-        __syncthreads();
-        if (warp == 0) {
-          for (int q = lane; q < nvg; q += 32)
-            bulk_s2g(p.y + (size_t)meta.pf[g0 + q] * N + nc0, y_s + (size_t)q * cfg.nc * 2, (uint32_t)ncn * 2);
-          bulk_commit();
-          bulk_wait_read_all();
-        }
-        __syncthreads();
       }
+      // Peers are done reading this CTA's partial t (and every thread with this
+      // group's shared memory) before the next group or block reuses it.
+      if (C > 1) cluster.sync(); else __syncthreads();
     }
+    if (nv > 0) phase ^= 1;
   }
-  if (warp == 0) bulk_wait_all();
-  // Keep every CTA of the cluster resident until its peers are done reading
-  // this CTA's shared memory.
-  if (C > 1) cluster.sync();
 }
 
-int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, CcCfg *cfg) {
+// Shared-memory layout for cluster size C; returns false if it does not fit.
+bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, CcCfg *cfg) {
   const int r = f.rank;
-  const long long item_bytes = (long long)(f.K + f.N) * r * 2;
-  int C = (int)((item_bytes + 24 * 1024 - 1) / (24 * 1024));
-  C = C < 1 ? 1 : (C > 8 ? 8 : C);
-  C = C > f.K / 8 ? f.K / 8 : C;
-  C = C > f.N / 8 ? f.N / 8 : C;
-  if (C < 1) C = 1;
-  const int kslice = (f.K / 8 + C - 1) / C * 8;
-  const int nslice = (f.N / 8 + C - 1) / C * 8;
-  int kc_max = ((64 * 1024) / (2 * r) - 8) / 8 * 8;
-  int nc_max = ((48 * 1024) / (2 * r)) / 8 * 8;
-  if (kc_max < 8) kc_max = 8;
-  if (nc_max < 8) nc_max = 8;
   cfg->C = C;
-  cfg->kc = kslice < kc_max ? kslice : kc_max;
-  cfg->nc = nslice < nc_max ? nslice : nc_max;
-  cfg->a_pitch = (cfg->kc + 8) * 2;
+  cfg->kslice = (f.K / 8 + C - 1) / C * 8;
+  cfg->nslice = (f.N / 8 + C - 1) / C * 8;
+  cfg->a_pitch = (cfg->kslice + 8) * 2;
   size_t off = (sizeof(Meta) + 127) / 128 * 128;
   cfg->off_a = (int)off;
   off += (size_t)r * cfg->a_pitch;
   cfg->off_x = (int)off;
-  off += (size_t)kPG * cfg->kc * 2;
+  off += (size_t)kPG * cfg->kslice * 2;
   off = (off + 127) / 128 * 128;
   cfg->off_b = (int)off;
-  off += (size_t)cfg->nc * r * 2;
+  off += (size_t)cfg->nslice * r * 2;
   off = (off + 127) / 128 * 128;
   cfg->off_y = (int)off;
-  off += (size_t)kPG * cfg->nc * 2;
+  off += (size_t)kPG * cfg->nslice * 2;
   off = (off + 127) / 128 * 128;
   cfg->off_tp = (int)off;
   off += (size_t)kPG * r * 4;
   cfg->off_tf = (int)off;
   off += (size_t)kPG * r * 4;
   cfg->smem_bytes = (int)off;
-  if ((size_t)cfg->smem_bytes > dev.max_smem_optin) return MOE_LORA_ERR_UNSUPPORTED;
-  return 0;
+  return (size_t)cfg->smem_bytes <= dev.max_smem_optin;
+}
+
+// Spread a block's adapter bytes over up to 16 CTAs: at least ~12 KB each
+// (so that each CTA is worth its launch, up to 8 CTAs) and at most ~48 KB each
+// (so that several CTAs share an SM); more CTAs if shared memory demands it.
+int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, CcCfg *cfg) {
+  const long long item_bytes = (long long)(f.K + f.N) * f.rank * 2;
+  const long long lo = (item_bytes + 48 * 1024 - 1) / (48 * 1024);
+  long long hi = (item_bytes + 12 * 1024 - 1) / (12 * 1024);
+  if (hi > 8) hi = 8;
+  long long want = lo > hi ? lo : hi;
+  const long long cmax = std::min<long long>(kMaxCluster, std::min(f.K / 8, f.N / 8));
+  if (want > cmax) want = cmax;
+  if (want < 1) want = 1;
+  for (long long C = want; C <= cmax; ++C)
+    if (layout(f, dev, (int)C, cfg)) return 0;
+  return MOE_LORA_ERR_UNSUPPORTED;
 }
 
 }  // namespace
@@ -386,28 +356,39 @@ int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, CcCfg *cfg) {
 int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = current_device_info(&dev)) return st;
-  if (f.num_active_loras > kMaxSlots || f.block_size > kMaxBlock) return MOE_LORA_ERR_UNSUPPORTED;
+  if (f.block_size > kMaxBlock) return MOE_LORA_ERR_UNSUPPORTED;
+  if (f.num_active_loras > 65535) return MOE_LORA_ERR_UNSUPPORTED;
   CcCfg cfg;
   if (int st = pick_cfg(f, dev, &cfg)) return st;
-  const long long bound = fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size);
-  if (bound <= 0) return 0;
-  const int G = (int)(bound < 65535 ? bound : 65535);
+  // Blocks one slot can produce: floor(M*topk / bs) full ones plus one partly
+  // filled block per non-empty expert segment.
+  const long long pairs = (long long)f.M * f.topk;
+  long long per_slot = pairs / f.block_size + (pairs < f.num_experts ? pairs : f.num_experts);
+  if (per_slot > f.max_num_m_blocks) per_slot = f.max_num_m_blocks;
+  if (per_slot > 65535) per_slot = 65535;
+  if (per_slot <= 0) return 0;
   const void *fn = (f.rank % 8 == 0) ? (const void *)fused_cuda_core_kernel<8>
                                      : (const void *)fused_cuda_core_kernel<4>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes) != cudaSuccess)
     return MOE_LORA_ERR_LAUNCH;
+  if (cfg.C > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return MOE_LORA_ERR_LAUNCH;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(cfg.C, G, 1);
+  lc.gridDim = dim3(cfg.C, f.num_active_loras, (unsigned)per_slot);
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = cfg.smem_bytes;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cfg.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // May start while the align kernel before it is finishing (it waits for it
+  // with griddepcontrol.wait before touching the align outputs).
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   cudaError_t err;
   if (f.rank % 8 == 0)
     err = cudaLaunchKernelEx(&lc, fused_cuda_core_kernel<8>, f, cfg);

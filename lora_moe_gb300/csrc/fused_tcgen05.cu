@@ -78,6 +78,7 @@ struct TcMeta {
   int slot_l[kMaxSlots];
   int prefix[kMaxSlots + 1];
   int epi_f[128];     // the current block's pair ids for the epilogue warps (-1 = padding)
+  int prod_f[128];    // the same for the producer warp (it may run one block ahead)
 };
 
 __device__ __forceinline__ int find_slot(const int *prefix, int nact, int item) {
@@ -115,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&meta.empty_sh[s], 1);
     }
     for (int s = 0; s < cfg.s_ex; ++s) {
-      mbar_init(&meta.full_ex[s], 1);
-      mbar_init(&meta.empty_ex[s], 2);
+      mbar_init(&meta.full_ex[s], 1 + 32);              // B tile (tx) + 32 lanes' y_in copies
+      mbar_init(&meta.empty_ex[s], 1 + kEpiThreads / 32); // MMA commit + epilogue warps
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&meta.tfull[a], 1);
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&meta.tmem_base, cfg.tmem_cols);
     tmem_relinquish();
   }
+  wait_for_prior_grid();   // align outputs are read from here on
   for (int z = tid; z < p.num_active_loras; z += kThreads) {
     const int l = __ldg(p.lora_ids + z);
     int nb = 0;
@@ -180,6 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // ======================= shrink: partial T over this CTA's K-slice
     if (warp == 0) {
+      for (int pr = lane; pr < BS; pr += 32) {
+        const int f = __ldg(ids + pr);
+        meta.prod_f[pr] = (f >= 0 && f < P) ? f : -1;
+      }
+      __syncwarp();
       // This lane gathers 16-byte chunk (lane % 8) of rows lane/8 + 4i.
       constexpr int kRowsPerLane = BS / 4;
       const int ch = lane & 7;
@@ -319,29 +326,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t *bt = ex_base + (size_t)s * cfg.ex_stage_bytes;
         uint8_t *yt = bt + cfg.yt_offset;
         const int n0 = nt * kTileN;
-        const int ncols = min(kTileN, N - n0);
-        // rows of y to load (same predicate as the copies below)
-        int mine = 0;
-        if (p.add_inputs)
-          for (int pr = lane; pr < BS; pr += 32) {
-            const int f = __ldg(ids + pr);
-            mine += (f >= 0 && f < P) ? 1 : 0;
-          }
-#pragma unroll
-        for (int d = 16; d > 0; d >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, d);
-        const int nrows = mine;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&meta.full_ex[s], (uint32_t)cfg.natoms * kTileN * 128 + (uint32_t)nrows * ncols * 2);
+          mbar_arrive_expect_tx(&meta.full_ex[s], (uint32_t)cfg.natoms * kTileN * 128);
           for (int a = 0; a < cfg.natoms; ++a)
             tma_load_3d(bt + a * (kTileN * 128), &tmap_b, a * 64, n0, le, &meta.full_ex[s]);
         }
-        __syncwarp();
-        if (p.add_inputs)
-          for (int pr = lane; pr < BS; pr += 32) {
-            const int f = __ldg(ids + pr);
-            if (f >= 0 && f < P)
-              bulk_g2s(yt + pr * (kTileN * 2), p.y + (size_t)f * N + n0, (uint32_t)ncols * 2, &meta.full_ex[s]);
-          }
+        // y_in rows: 16-byte chunks through the load/store unit (row pieces are
+        // too small for TMA to pay off); lane handles chunk (lane % 16) of rows
+        // lane/16 + 2i.
+        if (p.add_inputs) {
+          const int ch = lane & 15;
+          const int n = n0 + ch * 8;
+          if (n < N)
+            for (int pr = lane >> 4; pr < BS; pr += 2) {
+              const int f = meta.prod_f[pr];
+              if (f >= 0) cp_async_16(yt + pr * (kTileN * 2) + ch * 16, p.y + (size_t)f * N + n, 16u);
+            }
+        }
+        cp_async_mbar_arrive_noinc(&meta.full_ex[s]);
       }
     } else if (warp == 1) {
       if (lane == 0) {
@@ -409,27 +411,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        fence_proxy_async_cta();
         named_barrier(1, kEpiThreads);
-        if (warp == 2) {
-          const int ncols = min(kTileN, N - n0);
-          for (int pr = lane; pr < BS; pr += 32) {
-            const int f = meta.epi_f[pr];
-            if (f >= 0) bulk_s2g(p.y + (size_t)f * N + n0, yt + pr * (kTileN * 2), (uint32_t)ncols * 2);
-          }
-          bulk_commit();
-          bulk_wait_read_all();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&meta.empty_ex[s]);
+        // Write the finished rows back with 16-byte stores: thread handles chunk
+        // (etid % 16) of rows etid/16 + 16i.
+        {
+          const int etid = tid - 64;
+          const int ch = etid & 15;
+          const int n = n0 + ch * 8;
+          if (n < N)
+            for (int pr = etid >> 4; pr < BS; pr += kEpiThreads / 16) {
+              const int f = meta.epi_f[pr];
+              if (f >= 0)
+                *reinterpret_cast<uint4 *>(p.y + (size_t)f * N + n) =
+                    *reinterpret_cast<const uint4 *>(yt + pr * (kTileN * 2) + ch * 16);
+            }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta.empty_ex[s]);
       }
       // the next item rewrites epi_f only after every epilogue warp is done with it
       named_barrier(1, kEpiThreads);
     }
   }
 
-  // Drain: outstanding stores, then release tensor memory.
-  if (warp == 2) bulk_wait_all();
+  // Release tensor memory.
   tc_fence_before();
   __syncthreads();
   if (C > 1) cluster.sync();
@@ -540,13 +545,17 @@ int launch_bs(const FusedArgs &f, const TcCfg &cfg, const CUtensorMap &ta, const
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = cfg.smem_bytes;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cfg.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // May start while the align kernel before it is finishing (it waits for it
+  // with griddepcontrol.wait before touching the align outputs).
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   const cudaError_t err = cudaLaunchKernelEx(&lc, fused_tcgen05_kernel<BS>, ta, tb, f, cfg);
   return err == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
 }
