@@ -35,7 +35,8 @@
  *     NULL = the legacy default stream).  Nothing is synchronised.
  *   - The caller owns every buffer.  The library allocates no memory, keeps
  *     no per-call state between calls and may be called from several host
- *     threads.
+ *     threads (moe_lora_align_static_workspace, below, is the one exception:
+ *     it runs on a scratch buffer built into the library).
  *   - Return value: MOE_LORA_OK, or a moe_lora_status error code.  On an
  *     argument error nothing is enqueued.  Errors the device detects
  *     (out-of-range ids in device arrays, a wait that timed out) are OR-ed
@@ -182,6 +183,43 @@ int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lo
                                  int max_loras, int num_active_loras, int block_size,
                                  int max_num_tokens_padded, int max_num_m_blocks,
                                  int add_inputs, int path, int32_t *err_flag, void *stream);
+
+/* Size of the scratch buffer built into the library for
+ * moe_lora_align_static_workspace (4 MiB). */
+#define MOE_LORA_STATIC_WORKSPACE_BYTES ((size_t)4 << 20)
+
+/*
+ * moe_lora_align_static_workspace -- moe_lora_align (global-memory variant)
+ * for callers that cannot allocate device memory.
+ *
+ * vLLM's align has no counterpart to this entry point; it exists for callers
+ * that may not call cudaMalloc or any allocating routine where they align
+ * (code running under an allocator that forbids device allocations there,
+ * plugins that are handed only their input and output buffers, processes that
+ * must not grow device memory after start-up).  They pass the same inputs and
+ * outputs as to moe_lora_align; the workspace is a MOE_LORA_STATIC_WORKSPACE_BYTES
+ * buffer compiled into the library (every GPU that loads the library holds it
+ * until the process exits).  Nothing is allocated by this call.
+ *   - Same arguments, results and errors as moe_lora_align with
+ *     variant = MOE_LORA_ALIGN_GLOBAL, minus the workspace arguments.
+ *   - Returns MOE_LORA_ERR_WORKSPACE when
+ *     moe_lora_align_workspace_bytes(M, topk, num_experts, num_active_loras,
+ *     block_size, MOE_LORA_ALIGN_GLOBAL) exceeds MOE_LORA_STATIC_WORKSPACE_BYTES.
+ *   - The first call on each device (with that device current) looks up the
+ *     buffer's device address; make that first call before any stream capture.
+ *   - All calls on a device share the one buffer, which keeps the last call's
+ *     contents (no entry needs clearing between calls).  Calls that overlap on
+ *     the GPU -- on different streams, or from host threads without ordering
+ *     between them -- race on it and must not be issued.
+ */
+int moe_lora_align_static_workspace(const int32_t *topk_ids, const int32_t *token_lora_mapping,
+                                    const int32_t *lora_ids, const int32_t *adapter_enabled,
+                                    int M, int topk, int num_experts, int max_loras,
+                                    int num_active_loras, int block_size,
+                                    int32_t *sorted_token_ids, int32_t *expert_ids,
+                                    int32_t *num_tokens_post_padded,
+                                    int max_num_tokens_padded, int max_num_m_blocks,
+                                    int32_t *err_flag, void *stream);
 
 /* Human-readable name of a moe_lora_status value (static string). */
 const char *moe_lora_status_string(int status);

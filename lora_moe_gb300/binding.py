@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_align_workspace_bytes.argtypes = [I, I, I, I, I, I]
             L.moe_lora_align.restype = I
             L.moe_lora_align.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, I, I, P, S, I, P, P]
+            L.moe_lora_align_static_workspace.restype = I
+            L.moe_lora_align_static_workspace.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, I, I, P, P]
             L.moe_lora_fused_shrink_expand.restype = I
             L.moe_lora_fused_shrink_expand.argtypes = [P, P, P, P, P, P, P, P, P,
                                                        I, I, I, I, I, I, I, I, I, I, I, I, I, P, P]
@@ -122,6 +124,26 @@ def moe_lora_align(topk_ids, token_lora_mapping, lora_ids, num_experts, max_lora
         _ptr(workspace, None, "workspace"), ws_bytes, variant,
         _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
     _check(st, "moe_lora_align")
+
+
+STATIC_WORKSPACE_BYTES = 4 << 20
+
+
+def moe_lora_align_static_workspace(topk_ids, token_lora_mapping, lora_ids, num_experts, max_loras, block_size,
+                                    sorted_token_ids, expert_ids, num_tokens_post_padded, adapter_enabled=None,
+                                    err_flag=None, stream=None):
+    """moe_lora_align (global variant) on the library's built-in scratch buffer,
+    for callers that cannot allocate device memory; see include/moe_lora.h."""
+    M, topk = topk_ids.shape
+    st = lib().moe_lora_align_static_workspace(
+        _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(token_lora_mapping, torch.int32, "token_lora_mapping"),
+        _ptr(lora_ids, torch.int32, "lora_ids"), _ptr(adapter_enabled, torch.int32, "adapter_enabled"),
+        M, topk, num_experts, max_loras, lora_ids.numel(), block_size,
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(num_tokens_post_padded, torch.int32, "num_tokens_post_padded"),
+        sorted_token_ids.shape[-1], expert_ids.shape[-1],
+        _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+    _check(st, "moe_lora_align_static_workspace")
 
 
 def moe_lora_fused_shrink_expand(x, lora_a, lora_b, y, sorted_token_ids, expert_ids, num_tokens_post_padded,
