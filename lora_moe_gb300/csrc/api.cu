@@ -204,7 +204,8 @@ int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lo
   f.add_inputs = add_inputs ? 1 : 0;
   int use = path;
   if (use == MOE_LORA_PATH_AUTO)
-    use = ((long long)M * topk >= 1024 && rank % 8 == 0) ? MOE_LORA_PATH_TCGEN05 : MOE_LORA_PATH_CUDA_CORE;
+    use = ((long long)M * topk >= 1024 && tcgen05_path_supports(f)) ? MOE_LORA_PATH_TCGEN05
+                                                                     : MOE_LORA_PATH_CUDA_CORE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   return use == MOE_LORA_PATH_TCGEN05 ? launch_fused_tcgen05(f, s) : launch_fused_cuda_core(f, s);
 }

@@ -60,6 +60,9 @@ int launch_align_smem(const AlignArgs &a, cudaStream_t stream);
 int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream);
 int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream);
 int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream);
+// Whether the tensor-core path takes these arguments (rank % 8 == 0, at most
+// 128 listed slots).
+bool tcgen05_path_supports(const FusedArgs &f);
 
 // Device properties of the current device, cached per device.
 struct DeviceInfo {
