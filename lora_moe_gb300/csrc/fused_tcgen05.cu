@@ -52,7 +52,8 @@ constexpr int kMaxSlots = 128;
 constexpr int kTileK = 64;        // shrink K per stage (one 128-byte swizzle row)
 constexpr int kTileN = 128;       // expand output columns per tile (TMEM lanes)
 constexpr int kMmaRows = 128;     // M of every tcgen05.mma here
-constexpr int kMaxStages = 8;
+constexpr int kMaxStages = 12;
+constexpr int kMaxLag = 4;
 
 struct TcCfg {
   int r_pad;          // rank rounded up to 16, 32, 64 or 128
@@ -145,11 +146,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < cfg.s_ex; ++s) {
       mbar_init(&meta.full_ex[s], 1 + 32);
-      mbar_init(&meta.empty_ex[s], 1 + kEpiWarps);
+      mbar_init(&meta.empty_ex[s], 1 + kEpiWarps / 2);   // MMA commit + the 4 warps of one group
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&meta.tfull[a], 1);
-      mbar_init(&meta.tempty[a], kEpiWarps);
+      mbar_init(&meta.tempty[a], kEpiWarps / 2);       // accumulator a is drained by group a
       mbar_init(&meta.t_full[a], kEpiWarps);
       mbar_init(&meta.t_empty[a], 1);
     }
@@ -237,9 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // k-tiles are every other one): its copies are complete, and the fence
         // makes them visible to the tensor core's (async-proxy) reads.
         if (owned >= cfg.lag) {
-          if (cfg.lag == 0) cp_async_wait_group<0>();
-          else if (cfg.lag == 1) cp_async_wait_group<1>();
-          else cp_async_wait_group<2>();
+          switch (cfg.lag) {
+            case 0: cp_async_wait_group<0>(); break;
+            case 1: cp_async_wait_group<1>(); break;
+            case 2: cp_async_wait_group<2>(); break;
+            case 3: cp_async_wait_group<3>(); break;
+            default: cp_async_wait_group<4>(); break;
+          }
           fence_proxy_async_cta();
           mbar_arrive(&meta.full_sh[(sh_iter - 2 * cfg.lag) % cfg.s_sh]);
         }
@@ -305,14 +310,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (p.add_inputs) {
           // y_in rows through the load/store unit: lane takes 16-byte chunk
-          // (lane % 16) of rows lane/16 + 2i.
+          // (lane % 16) of rows lane/16 + 2i; the row ids are read before any
+          // copy is issued so that the copies go out back to back.
           const int c16 = lane & 15;
           const int nn = n0 + c16 * 8;
-          if (nn < N)
-            for (int pr = lane >> 4; pr < BS; pr += 2) {
-              const int f = meta.prod_f[pr];
-              if (f >= 0) cp_async_16(yt + pr * (kTileN * 2) + c16 * 16, p.y + (size_t)f * N + nn, 16u);
-            }
+          if (nn < N) {
+            constexpr int kRows = BS / 2;
+            int fr[kRows];
+#pragma unroll
+            for (int i = 0; i < kRows; ++i) fr[i] = meta.prod_f[(lane >> 4) + 2 * i];
+#pragma unroll
+            for (int i = 0; i < kRows; ++i)
+              if (fr[i] >= 0)
+                cp_async_16(yt + ((lane >> 4) + 2 * i) * (kTileN * 2) + c16 * 16, p.y + (size_t)fr[i] * N + nn, 16u);
+          }
         }
         cp_async_mbar_arrive_noinc(&meta.full_ex[s]);
       }
@@ -352,10 +363,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ======================= epilogue warps 2..9
+    // Two groups of four warps (h = 0: warps 2..5, h = 1: warps 6..9), one warp
+    // per TMEM lane quarter each.  Both read the shrink accumulator; for the
+    // expand, group h takes the tiles that land in accumulator h (every other
+    // tile), so one group's TMEM loads overlap the other group's stores.
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int etid = tid - 64;
-    constexpr int kHalf = BS / 2;
-    constexpr int kStoreRows = BS / 16;      // rows a thread stores per tile
+    const int gtid = etid & 127;             // thread index inside the group
+    constexpr int kCR = BS < 32 ? BS : 32;   // rows per piece of a tile
+    constexpr int kChunks = BS / kCR;
+    constexpr int kStoreRows = BS / 8;       // rows a thread stores per tile
     uint32_t ex_iter = 0, acc_iter = 0;
     int kk = 0;
     for (int gb = gb0; gb <= gb1; ++gb, ++kk) {
@@ -370,12 +387,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         meta.epi_f[etid] = v;
       }
       named_barrier(1, kEpiThreads);
-      uint64_t valid = 0;   // bit i: row h*kHalf + i is a real pair
+      uint32_t valid[kChunks];   // bit i of valid[c]: row kCR*c + i is a real pair
 #pragma unroll
-      for (int i = 0; i < kHalf; ++i) valid |= (uint64_t)(meta.epi_f[h * kHalf + i] >= 0) << i;
+      for (int c = 0; c < kChunks; ++c) {
+        valid[c] = 0;
+#pragma unroll
+        for (int i = 0; i < kCR; ++i) valid[c] |= (uint32_t)(meta.epi_f[kCR * c + i] >= 0) << i;
+      }
       int st_f[kStoreRows];
 #pragma unroll
-      for (int i = 0; i < kStoreRows; ++i) st_f[i] = meta.epi_f[(etid >> 4) + 16 * i];
+      for (int i = 0; i < kStoreRows; ++i) st_f[i] = meta.epi_f[(gtid >> 4) + 8 * i];
 
       // -- shrink readout: T (fp32 in TMEM) -> T_hi, T_lo (bf16, swizzled) in buffer tb
       const int tb = kk % cfg.t_bufs;
@@ -421,50 +442,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&meta.shrink_free);
       }
 
-      // -- expand epilogue, tile by tile
+      // -- expand epilogue: this group's tiles of the block
       for (int nt = tile_lo(gb); nt < tile_hi(gb); ++nt, ++ex_iter, ++acc_iter) {
+        if ((int)(acc_iter & 1) != h) continue;
         const int s = ex_iter % cfg.s_ex;
-        const int a = acc_iter & 1;
+        const int a = h;
         mbar_wait(&meta.tfull[a], (acc_iter >> 1) & 1, abort, p.err);
         tc_fence_after();
-        float v[kHalf];
-#pragma unroll
-        for (int c0 = 0; c0 < kHalf; c0 += 8) {
-          float w8[8];
-          tmem_ld8(tmem + a * BS + ((uint32_t)(32 * q) << 16) + h * kHalf + c0, w8);
-#pragma unroll
-          for (int i = 0; i < 8; ++i) v[c0 + i] = w8[i];
-        }
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&meta.tempty[a]);
         mbar_wait(&meta.full_ex[s], (ex_iter / cfg.s_ex) & 1, abort, p.err);
         uint8_t *yt = ex_base + (size_t)s * cfg.ex_stage + cfg.yt_off;
         const int n0 = nt * kTileN;
         const int nl = 32 * q + lane;
-        if (n0 + nl < N) {
-          uint16_t *col = reinterpret_cast<uint16_t *>(yt + (size_t)h * kHalf * (kTileN * 2)) + nl;
-          if (p.add_inputs) {
-            uint16_t old[kHalf];   // all loads first, then all stores
+        const bool col_ok = n0 + nl < N;
+        uint16_t *col = reinterpret_cast<uint16_t *>(yt) + nl;
 #pragma unroll
-            for (int i = 0; i < kHalf; ++i) old[i] = col[i * kTileN];
+        for (int c = 0; c < kChunks; ++c) {
+          float v[kCR];
 #pragma unroll
-            for (int i = 0; i < kHalf; ++i) v[i] += bf16_bits_to_float(old[i]);
+          for (int c0 = 0; c0 < kCR; c0 += 8) {
+            float w8[8];
+            tmem_ld8(tmem + a * BS + ((uint32_t)(32 * q) << 16) + kCR * c + c0, w8);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[c0 + i] = w8[i];
           }
+          tc_wait_ld();
+          if (col_ok) {
+            if (p.add_inputs) {
+              uint16_t old[kCR];   // all loads first, then all stores
 #pragma unroll
-          for (int i = 0; i < kHalf; ++i)
-            if ((valid >> i) & 1) col[i * kTileN] = float_to_bf16_bits(v[i]);
+              for (int i = 0; i < kCR; ++i) old[i] = col[(kCR * c + i) * kTileN];
+#pragma unroll
+              for (int i = 0; i < kCR; ++i) v[i] += bf16_bits_to_float(old[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < kCR; ++i)
+              if ((valid[c] >> i) & 1) col[(kCR * c + i) * kTileN] = float_to_bf16_bits(v[i]);
+          }
         }
-        named_barrier(1, kEpiThreads);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta.tempty[a]);
+        named_barrier(2 + h, kEpiThreads / 2);
         {
-          const int c16 = etid & 15;
+          // write the finished rows back: thread takes 16-byte chunk (gtid % 16)
+          // of rows gtid/16 + 8i
+          const int c16 = gtid & 15;
           const int nn = n0 + c16 * 8;
           if (nn < N) {
             uint4 vals[kStoreRows];
 #pragma unroll
             for (int i = 0; i < kStoreRows; ++i)
-              vals[i] = *reinterpret_cast<const uint4 *>(yt + ((etid >> 4) + 16 * i) * (kTileN * 2) + c16 * 16);
+              vals[i] = *reinterpret_cast<const uint4 *>(yt + ((gtid >> 4) + 8 * i) * (kTileN * 2) + c16 * 16);
 #pragma unroll
             for (int i = 0; i < kStoreRows; ++i)
               if (st_f[i] >= 0) *reinterpret_cast<uint4 *>(p.y + (size_t)st_f[i] * N + nn) = vals[i];
@@ -538,11 +566,11 @@ int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, TcCfg *cfg) {
   const int meta_bytes = round_up((int)sizeof(TcMeta), 1024);
   const int budget = (int)dev.max_smem_optin;
   // Pick the plan with the most bytes in flight (shrink stages in flight are
-  // 2 * (lag + 1): two producer warps, each `lag` stages ahead).
+  // 2 * (lag + 1): two producer warps, each up to `lag` stages ahead).
   int best = -1 << 30;
   TcCfg pick = *cfg;
   for (int s_sh = kMaxStages; s_sh >= 2; --s_sh) {
-    const int lag = std::min(2, (s_sh - 1) / 2);
+    const int lag = std::min(kMaxLag, (s_sh - 1) / 2);
     for (int s_ex = kMaxStages; s_ex >= 1; --s_ex) {
       for (int t_bufs = 2; t_bufs >= 1; --t_bufs) {
         const int after_sh = s_ex * cfg->ex_stage + t_bufs * 2 * cfg->t_part + meta_bytes;
@@ -552,7 +580,7 @@ int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, TcCfg *cfg) {
         // (never used) must still lie inside the allocation
         if (cfg->sh_stage + after_sh < 128 * 128) continue;
         const int sh_fly = std::min(s_sh, 2 * (lag + 1)) * cfg->sh_stage;
-        const int score = std::min(sh_fly, 112 * 1024) + std::min(s_ex * cfg->ex_stage, 128 * 1024) +
+        const int score = std::min(sh_fly, 128 * 1024) + std::min(s_ex * cfg->ex_stage, 128 * 1024) +
                           (t_bufs == 2 ? 8 * 1024 : 0) - total / 64;
         if (score > best) {
           best = score;
