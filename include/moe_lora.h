@@ -81,8 +81,12 @@ typedef enum {
 
 /* Fused paths (moe_lora_fused_shrink_expand `path`). */
 #define MOE_LORA_PATH_AUTO 0
-#define MOE_LORA_PATH_CUDA_CORE 1 /* decode-sized blocks: CUDA cores, warp-shuffle reductions */
+#define MOE_LORA_PATH_CUDA_CORE 1 /* decode-sized blocks on CUDA cores (the cluster kernel below) */
 #define MOE_LORA_PATH_TCGEN05 2   /* prefill-sized blocks: tcgen05 tensor-core MMAs */
+#define MOE_LORA_PATH_CUDA_CORE_CLUSTER 3 /* CUDA cores: a thread-block cluster per block, K split over
+                                             its CTAs, partial t summed through distributed shared memory */
+#define MOE_LORA_PATH_CUDA_CORE_STREAM 4  /* CUDA cores: persistent CTAs stream balanced tile ranges
+                                             (rank % 8 == 0, block_size * rank <= 2048) */
 
 /* Capacity of one LoRA row of sorted_token_ids: every pair once plus up to
  * block_size-1 padding slots for each expert: M*topk + num_experts*(block_size-1).
@@ -172,7 +176,8 @@ int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping,
  * rank % 8 == 0); K % 8 == 0 and N % 8 == 0; x, lora_a, lora_b, y 16-byte
  * aligned; other limits as for moe_lora_align.  path: MOE_LORA_PATH_*; AUTO
  * picks the CUDA-core path for decode-sized batches (M*topk < 1024) and the
- * tensor-core path otherwise (when rank % 8 == 0).
+ * tensor-core path otherwise (when rank % 8 == 0); MOE_LORA_PATH_CUDA_CORE
+ * runs the cluster kernel (MOE_LORA_PATH_CUDA_CORE_CLUSTER).
  */
 int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a,
                                  const moe_lora_bf16 *lora_b, moe_lora_bf16 *y,

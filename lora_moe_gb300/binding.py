@@ -18,7 +18,7 @@ from . import build as _build
 
 MOE_LORA_OK = 0
 ALIGN_AUTO, ALIGN_SMEM, ALIGN_GLOBAL = 0, 1, 2
-PATH_AUTO, PATH_CUDA_CORE, PATH_TCGEN05 = 0, 1, 2
+PATH_AUTO, PATH_CUDA_CORE, PATH_TCGEN05, PATH_CUDA_CORE_CLUSTER, PATH_CUDA_CORE_STREAM = 0, 1, 2, 3, 4
 DEVERR_EXPERT_ID, DEVERR_LORA_ID, DEVERR_CAPACITY, DEVERR_PAIR_ID, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 
 _lib = None

@@ -96,10 +96,12 @@ __device__ __forceinline__ void warp_scatter(const AlignArgs &a, int l, int lo, 
   }
 }
 
-// Exclusive scan of one int per thread across a 1024-thread CTA; returns the
-// thread's exclusive prefix and writes the total to *total.
-__device__ __forceinline__ int block_exclusive_scan_1024(int v, int *warp_sums, int *total) {
+// Exclusive scan of one int per thread across the CTA (blockDim.x a multiple
+// of 32, at most 1024); returns the thread's exclusive prefix and writes the
+// total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
   int incl = v;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -109,7 +111,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int *warp_sums, 
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int s = warp_sums[lane];
+    int s = lane < nwarps ? warp_sums[lane] : 0;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
       const int t = __shfl_up_sync(0xffffffffu, s, d);
@@ -119,20 +121,20 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int *warp_sums, 
   }
   __syncthreads();
   const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
-  *total = warp_sums[31];
+  *total = warp_sums[nwarps - 1];
   return excl;
 }
 
 // Given per-expert counts cnt[e] (e < E, one per thread), compute segment
 // offsets off[0..E], write num_tokens_post_padded[l], the padding sentinels and
 // expert_ids.  Returns false (uniformly) when the result exceeds the caller's
-// capacity.  Called by all 1024 threads.
+// capacity.  Called by every thread of a CTA of at least E threads.
 __device__ bool write_segments(const AlignArgs &a, int l, const int *cnt, int *off, int *warp_sums) {
   const int E = a.num_experts, bs = a.block_size, tid = threadIdx.x;
   const int c = (tid < E) ? cnt[tid] : 0;
   const int padded = (c + bs - 1) / bs * bs;
   int total;
-  const int excl = block_exclusive_scan_1024(padded, warp_sums, &total);
+  const int excl = block_exclusive_scan(padded, warp_sums, &total);
   if (tid < E) off[tid] = excl;
   if (tid == 0) off[E] = total;
   __syncthreads();
@@ -205,9 +207,10 @@ __device__ __forceinline__ void warp_scatter_cached(int lo, int hi, int *tab, in
   }
 }
 
-// One CTA of 1024 threads per active slot.  The pairs are split over the
-// first W warps (W = min(32, ceil(P / 32))), each a contiguous range; the
-// per-warp counters form a W x E table in shared memory.
+// One CTA per active slot, of max(32 W, E) threads rounded up to a warp: the
+// pairs are split over the first W warps (W = min(32, ceil(P / 32))), each a
+// contiguous range, and the per-warp counters form a W x E table in shared
+// memory; one thread per expert does the column scan.
 __global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const AlignArgs a) {
   extern __shared__ int smem[];
   const int E = a.num_experts;
@@ -226,7 +229,7 @@ __global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const Align
   const int l = slot_lora(a, blockIdx.x, tid == 0);
   if (l < 0) return;
 
-  for (int i = tid; i < W * E; i += kSmemThreads) tab[i] = 0;
+  for (int i = tid; i < W * E; i += blockDim.x) tab[i] = 0;
   __syncthreads();
 
   const int per_warp = ((P + W - 1) / W + 31) / 32 * 32;
@@ -393,8 +396,9 @@ int launch_align_smem(const AlignArgs &a, cudaStream_t stream) {
   const long long P = (long long)a.M * a.topk;
   const int W = (int)std::max(1LL, std::min<long long>(kSmemWarps, (P + 31) / 32));
   const size_t bytes = ((size_t)W * a.num_experts + 2 * (size_t)a.num_experts + 1 + 32) * sizeof(int);
+  const int threads = std::min(kSmemThreads, (std::max(32 * W, a.num_experts) + 31) / 32 * 32);
   if (int st = set_smem_limit((const void *)align_smem_kernel, bytes)) return st;
-  align_smem_kernel<<<a.num_active_loras, kSmemThreads, bytes, stream>>>(a);
+  align_smem_kernel<<<a.num_active_loras, threads, bytes, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
 }
 

@@ -171,8 +171,9 @@ int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lo
   if (K < 8 || N < 8 || rank < 1) return MOE_LORA_ERR_INVALID_ARG;
   if (rank > kMaxRank || rank % 4 != 0) return MOE_LORA_ERR_UNSUPPORTED;
   if (K % 8 != 0 || N % 8 != 0) return MOE_LORA_ERR_MISALIGNED;
-  if (path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_TCGEN05) return MOE_LORA_ERR_INVALID_ARG;
-  if (path == MOE_LORA_PATH_TCGEN05 && rank % 8 != 0) return MOE_LORA_ERR_UNSUPPORTED;
+  if (path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_CUDA_CORE_STREAM) return MOE_LORA_ERR_INVALID_ARG;
+  if ((path == MOE_LORA_PATH_TCGEN05 || path == MOE_LORA_PATH_CUDA_CORE_STREAM) && rank % 8 != 0)
+    return MOE_LORA_ERR_UNSUPPORTED;
   if ((long long)M * K > INT32_MAX * 8LL || (long long)M * topk * N > INT32_MAX * 8LL)
     return MOE_LORA_ERR_UNSUPPORTED;
   if (num_active_loras == 0 || M == 0) return MOE_LORA_OK;
@@ -206,8 +207,16 @@ int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lo
   if (use == MOE_LORA_PATH_AUTO)
     use = ((long long)M * topk >= 1024 && tcgen05_path_supports(f)) ? MOE_LORA_PATH_TCGEN05
                                                                      : MOE_LORA_PATH_CUDA_CORE;
+  // On every decode workload measured, the cluster kernel beat the streaming
+  // one (the streaming kernel recomputes the shrink of a block in every CTA
+  // whose tile range touches it), so the CUDA-core choice is the cluster kernel.
+  if (use == MOE_LORA_PATH_CUDA_CORE) use = MOE_LORA_PATH_CUDA_CORE_CLUSTER;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return use == MOE_LORA_PATH_TCGEN05 ? launch_fused_tcgen05(f, s) : launch_fused_cuda_core(f, s);
+  switch (use) {
+    case MOE_LORA_PATH_TCGEN05: return launch_fused_tcgen05(f, s);
+    case MOE_LORA_PATH_CUDA_CORE_STREAM: return launch_fused_stream_cc(f, s);
+    default: return launch_fused_cuda_core(f, s);
+  }
 }
 
 }  // extern "C"

@@ -111,8 +111,15 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
   }
   if (p.adapter_enabled && __ldg(p.adapter_enabled + l) == 0) return;
   wait_for_prior_grid();   // align outputs are read from here on
+  // The first block's expert and pair ids are requested together with the
+  // slot's block count (one round trip); they are only used if the block exists.
+  const int b_first = blockIdx.z;
+  const int e_first = __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b_first);
+  int f_first = -1;
+  if (tid < bs && b_first * bs + tid < p.max_num_tokens_padded)
+    f_first = __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + b_first * bs + tid);
   const int nblocks = min(__ldg(p.num_tokens_post_padded + l) / bs, p.max_num_m_blocks);
-  if ((int)blockIdx.z >= nblocks) return;
+  if (b_first >= nblocks) return;
 
   if (tid == 0) {
     mbar_init(&meta.bar, 1);
@@ -129,14 +136,14 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
   const int n_lo = (c * n8 / C) * 8, n_hi = ((c + 1) * n8 / C) * 8;
   const int kn = k_hi - k_lo, nn = n_hi - n_lo;
 
-  for (int b = blockIdx.z; b < nblocks; b += gridDim.z) {
-    const int e = __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b);
+  for (int b = b_first; b < nblocks; b += gridDim.z) {
+    const int e = b == b_first ? e_first : __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b);
     // Compact the block's real pairs, keeping their order.
     {
       const int idx = b * bs + tid;
       int f = -1;
       if (tid < bs && idx < p.max_num_tokens_padded) {
-        f = __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + idx);
+        f = b == b_first ? f_first : __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + idx);
         if (f < 0 || f > P) {
           if (c == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
           f = -1;
@@ -365,6 +372,10 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   const long long pairs = (long long)f.M * f.topk;
   long long per_slot = pairs / f.block_size + (pairs < f.num_experts ? pairs : f.num_experts);
   if (per_slot > f.max_num_m_blocks) per_slot = f.max_num_m_blocks;
+  // Blocks a slot really has are usually far fewer than that bound; past a few
+  // waves of clusters, CTAs walk several blocks instead of launching empty.
+  const long long cap = std::max<long long>(48, 4LL * dev.sm_count / ((long long)cfg.C * f.num_active_loras));
+  if (per_slot > cap) per_slot = cap;
   if (per_slot > 65535) per_slot = 65535;
   if (per_slot <= 0) return 0;
   const void *fn = (f.rank % 8 == 0) ? (const void *)fused_cuda_core_kernel<8>

@@ -63,6 +63,9 @@ int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream);
 // Whether the tensor-core path takes these arguments (rank % 8 == 0, at most
 // 128 listed slots).
 bool tcgen05_path_supports(const FusedArgs &f);
+// The CUDA-core streaming kernel (decode-sized blocks, large adapters).
+int launch_fused_stream_cc(const FusedArgs &f, cudaStream_t stream);
+bool stream_cc_supports(const FusedArgs &f);
 
 // Device properties of the current device, cached per device.
 struct DeviceInfo {

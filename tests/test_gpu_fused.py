@@ -22,6 +22,18 @@ def _cuda():
         pytest.skip("no CUDA device")
 
 
+ALL_PATHS = [B.PATH_CUDA_CORE_CLUSTER, B.PATH_CUDA_CORE_STREAM, B.PATH_TCGEN05]
+
+
+def skip_unsupported(w, path):
+    """The streaming CUDA-core kernel and the tensor-core kernel need rank % 8 == 0;
+    the streaming kernel also block_size * rank <= 2048."""
+    if path in (B.PATH_TCGEN05, B.PATH_CUDA_CORE_STREAM) and w.rank % 8:
+        pytest.skip("path needs rank % 8 == 0")
+    if path == B.PATH_CUDA_CORE_STREAM and w.block_size * w.rank > 2048:
+        pytest.skip("streaming CUDA-core kernel needs block_size * rank <= 2048")
+
+
 def run_and_compare_full(inp, path, add_inputs=True, adapter_enabled=None, variant=B.ALIGN_AUTO):
     from helpers import DeviceInputs, gpu_step, host_bf16_bits, check_close, covered
     d = DeviceInputs(inp, variant)
@@ -36,9 +48,10 @@ def run_and_compare_full(inp, path, add_inputs=True, adapter_enabled=None, varia
 
 
 @pytest.mark.parametrize("add_inputs", [True, False])
-@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05, B.PATH_AUTO])
+@pytest.mark.parametrize("path", ALL_PATHS + [B.PATH_CUDA_CORE, B.PATH_AUTO])
 @pytest.mark.parametrize("name", ["tiny", "decode_qwen3_w13", "decode_gptoss_w2"])
 def test_fused_small_workloads_full(name, path, add_inputs):
+    skip_unsupported(gen.WORKLOADS[name], path)
     inp = gen.make_inputs(gen.WORKLOADS[name])
     run_and_compare_full(inp, path, add_inputs)
 
@@ -55,11 +68,12 @@ def small_workload(seed, **kw):
     return gen.Workload(**base)
 
 
-@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("path", ALL_PATHS)
 @pytest.mark.parametrize("seed", range(12))
 def test_fused_random_shapes(seed, path):
     """Ragged K (not a multiple of the 64-wide K tile) and N (not a multiple of
     the 128-wide N tile), every block size, ranks 8..128."""
+    skip_unsupported(small_workload(seed), path)
     inp = gen.make_inputs(small_workload(seed))
     run_and_compare_full(inp, path, add_inputs=bool(seed % 2))
 
@@ -67,17 +81,19 @@ def test_fused_random_shapes(seed, path):
 @pytest.mark.parametrize("rank", [4, 12, 20])
 def test_fused_small_ranks_cuda_core(rank):
     inp = gen.make_inputs(small_workload(77, rank=rank, K=136, N=264))
-    run_and_compare_full(inp, B.PATH_CUDA_CORE)
+    run_and_compare_full(inp, B.PATH_CUDA_CORE_CLUSTER)
 
 
-@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("path", ALL_PATHS)
 @pytest.mark.parametrize("rank", [8, 16, 64, 128])
 def test_fused_ranks(rank, path):
-    inp = gen.make_inputs(small_workload(5, rank=rank, M=96, K=520, N=392, E=6, topk=2, block_size=32))
+    w = small_workload(5, rank=rank, M=96, K=520, N=392, E=6, topk=2, block_size=32)
+    skip_unsupported(w, path)
+    inp = gen.make_inputs(w)
     run_and_compare_full(inp, path)
 
 
-@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("path", ALL_PATHS)
 @pytest.mark.parametrize("rank,nnz", [(8, 16), (16, 8), (64, 2), (128, 1)])
 def test_fused_exact_integer_case(path, rank, nnz):
     """x, B in {-1, 0, 1}; each row of A has nnz entries in {-1, 1}; y_in in
@@ -89,7 +105,8 @@ def test_fused_exact_integer_case(path, rank, nnz):
     the tails."""
     from helpers import DeviceInputs, gpu_step, host_bf16_bits
     w = gen.Workload("int", M=70, K=264, N=392, E=3, topk=2, max_loras=2, num_active_loras=2, rank=rank,
-                     block_size=64, mapping="uniform_with_none", experts="uniform", seed=3)
+                     block_size=64 if path != B.PATH_CUDA_CORE_STREAM else 16, mapping="uniform_with_none",
+                     experts="uniform", seed=3)
     inp = gen.make_inputs(w)
     rng = np.random.default_rng(8)
     f2b = gen.f32_to_bf16_bits
@@ -114,7 +131,7 @@ def test_fused_exact_integer_case(path, rank, nnz):
             tuple(np.argwhere(bad)[0]), got[bad][0], ref[bad][0])
 
 
-@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("path", ALL_PATHS)
 def test_fused_disabled_adapter_and_poison(path):
     """Inactive and disabled slots hold NaN in A and B; the output stays finite
     and their tokens keep y_in."""
@@ -128,7 +145,7 @@ def test_fused_disabled_adapter_and_poison(path):
     run_and_compare_full(inp, path, adapter_enabled=enabled)
 
 
-@pytest.mark.parametrize("path", [B.PATH_CUDA_CORE, B.PATH_TCGEN05])
+@pytest.mark.parametrize("path", ALL_PATHS)
 def test_fused_no_covered_pairs(path):
     from helpers import DeviceInputs, gpu_step, host_bf16_bits
     w = gen.Workload("none", M=40, K=64, N=128, E=4, topk=2, max_loras=2, num_active_loras=2, rank=8,
@@ -184,7 +201,13 @@ def test_fused_full_size_sampled(name):
 
 
 def test_fused_prefill_full_size_cuda_core_sampled():
-    """The CUDA-core path on the prefill shape (it is not the path AUTO picks
-    there, but it must be correct on it)."""
+    """The CUDA-core cluster kernel on the prefill shape (it is not the path AUTO
+    picks there, but it must be correct on it)."""
     inp = gen.make_inputs(gen.WORKLOADS["prefill_mixtral_w13"])
-    sampled_compare(inp, B.PATH_CUDA_CORE, add_inputs=False, n_pairs=24)
+    sampled_compare(inp, B.PATH_CUDA_CORE_CLUSTER, add_inputs=False, n_pairs=24)
+
+
+def test_fused_prefill_full_size_stream_cc_sampled():
+    """The streaming CUDA-core kernel on the prefill shape (block 64 x rank 16)."""
+    inp = gen.make_inputs(gen.WORKLOADS["prefill_mixtral_w13"])
+    sampled_compare(inp, B.PATH_CUDA_CORE_STREAM, add_inputs=True, n_pairs=24)
