@@ -16,6 +16,12 @@ the launching stream; the max over ranks is reported.  Kernel-level durations
 Launch under torchrun for N > 1: every rank runs its own replica (the path has
 no exchange step); rank 0 prints the JSON line.
 
+Options of the general fused call (moe_lora_fused_shrink_expand_ex), off by
+default: --slices S (separate adapters per slice, e.g. 2 for w13's gate and
+up), --per-pair-x (one input row per pair, the w2 stage), --routed-weight
+(delta scaled by the router weight).  With any of them the step runs the
+general call instead of the plain one.
+
 --impl reference times the CPU oracle (test infrastructure) on the host cores
 instead, on a bounded sample of pairs per step, scaled to microseconds per
 full step.
@@ -53,19 +59,37 @@ def parse():
                     help="device time spent on each kernel-level timing")
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="only run W + this many eager steps (for ncu); prints no JSON line")
-    ap.add_argument("--path", type=int, default=0, help="fused path: 0 auto, 1 CUDA cores, 2 tcgen05")
+    ap.add_argument("--path", type=int, default=0, help="fused path: 0 auto, 1 CUDA cores, 2 tcgen05, 3 CUDA-core cluster, 4 CUDA-core streaming")
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0: enough to exceed 3x L2)")
+    ap.add_argument("--slices", type=int, default=1, help="adapter slices per layer (general call)")
+    ap.add_argument("--per-pair-x", action="store_true", help="one input row per pair (general call)")
+    ap.add_argument("--routed-weight", action="store_true", help="scale by the router weight (general call)")
     return ap.parse_args()
+
+
+def uses_ex(args):
+    return args.slices != 1 or args.per_pair_x or args.routed_weight
+
+
+def make_step_inputs(w, args):
+    """(routing inputs, general-call inputs or None)."""
+    if not uses_ex(args):
+        return gen.make_inputs(w), None
+    ex = gen.make_ex_inputs(w, num_slices=args.slices, x_per_pair=args.per_pair_x,
+                            routed_weights=args.routed_weight)
+    return ex.base, ex
 
 
 # --------------------------------------------------------------------------- roofline bookkeeping
 
-def algorithmic_counts(inp: gen.Inputs):
+def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weight=False):
     """What the method must move / compute for one step, from the actual inputs.
 
-    bytes = x rows of covered tokens once + A and B of every touched (lora,
-    expert) segment once + y read and write of covered pairs + align metadata;
-    flops = 2 r (K + N) per covered pair."""
+    bytes = x rows of covered tokens (or covered pairs, with one input row per
+    pair) once + A and B of every touched (lora, expert) segment once per slice
+    + y read and write of covered pairs' slice columns + router weights of
+    covered pairs + align metadata; flops = 2 r (K + N) per covered pair and
+    slice."""
     w = inp.w
     act = set(int(v) for v in inp.lora_ids)
     m_cov = np.array([int(l) in act for l in inp.token_lora_mapping])
@@ -79,11 +103,12 @@ def algorithmic_counts(inp: gen.Inputs):
     padded = sum(-(-c // w.block_size) * w.block_size for c in segs.values())
     blocks = padded // w.block_size
     r = w.rank
-    fused_bytes = (2 * w.K * int(m_cov.sum()) + S * 2 * r * (w.K + w.N) + P * w.N * 2 * 2
-                   + 4 * (padded + blocks + w.num_active_loras))
+    x_rows = P if per_pair_x else int(m_cov.sum())
+    fused_bytes = (2 * w.K * x_rows + slices * S * 2 * r * (w.K + w.N) + slices * P * w.N * 2 * 2
+                   + (4 * P if routed_weight else 0) + 4 * (padded + blocks + w.num_active_loras))
     align_bytes = 4 * w.M * w.topk + 4 * w.M + 4 * (padded + blocks + w.num_active_loras)
     return dict(pairs=P, segments=S, padded_rows=padded, blocks=blocks, fused_bytes=fused_bytes,
-                align_bytes=align_bytes, flops=2 * r * (w.K + w.N) * P)
+                align_bytes=align_bytes, flops=2 * r * (w.K + w.N) * P * slices)
 
 
 def measured_peaks():
@@ -187,9 +212,10 @@ def max_over_ranks(pg, value, use_cuda):
 
 # --------------------------------------------------------------------------- CPU oracle timing
 
-def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: int = None):
+def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: int = None, ex=None):
     """Time the oracle's align (whole batch) and fused stage (a rotating subset
-    of covered pairs, every column) and scale to microseconds per full step.
+    of covered pairs, every column; the general definition when `ex` holds the
+    general call's inputs) and scale to microseconds per full step.
 
     Returns (us_per_step, description, calls_made)."""
     import oracle
@@ -208,7 +234,11 @@ def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: in
         oracle.align(inp.topk_ids, inp.token_lora_mapping, inp.lora_ids, w.E, w.max_loras, w.block_size)
         t1 = time.perf_counter()
         sel = cov_idx[(made * n + np.arange(n)) % max(1, len(cov_idx))] if len(cov_idx) else cov_idx
-        if len(sel):
+        if len(sel) and ex is not None:
+            oracle.fused_ex(ex.x, ex.lora_a, ex.lora_b, ex.y_in, inp.topk_ids, inp.token_lora_mapping,
+                            inp.lora_ids, topk_weights=ex.topk_weights, x_per_pair=ex.x_per_pair,
+                            y_offset=ex.y_offset, pairs=sel)
+        elif len(sel):
             oracle.fused_sampled(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
                                  inp.lora_ids, sel, cols)
         t2 = time.perf_counter()
@@ -237,8 +267,8 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = gen.WORKLOADS[args.workload]
-    inp = gen.make_inputs(w)
-    counts = algorithmic_counts(inp)
+    inp, ex = make_step_inputs(w, args)
+    counts = algorithmic_counts(inp, args.slices, args.per_pair_x, args.routed_weight)
 
     def i32(a):
         return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
@@ -247,11 +277,19 @@ def run_ours(args, world, rank, local, pg):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
 
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    per_set = (inp.x.nbytes + inp.lora_a.nbytes + inp.lora_b.nbytes + 2 * inp.y_in.nbytes +
+    src = ex if ex is not None else inp
+    a_list = src.lora_a if ex is not None else [inp.lora_a]
+    b_list = src.lora_b if ex is not None else [inp.lora_b]
+    per_set = (src.x.nbytes + sum(a.nbytes for a in a_list) + sum(b.nbytes for b in b_list) + 2 * src.y_in.nbytes +
                inp.topk_ids.nbytes + inp.token_lora_mapping.nbytes)
     NB = args.sets if args.sets > 0 else int(max(2, min(64, -(-3 * l2 // per_set))))
     base = dict(topk_ids=i32(inp.topk_ids), mapping=i32(inp.token_lora_mapping), lora_ids=i32(inp.lora_ids),
-                x=bf16(inp.x), a=bf16(inp.lora_a), b=bf16(inp.lora_b), y=bf16(inp.y_in))
+                x=bf16(src.x), y=bf16(src.y_in))
+    for i, (a, b) in enumerate(zip(a_list, b_list)):
+        base["a%d" % i] = bf16(a)
+        base["b%d" % i] = bf16(b)
+    if ex is not None and ex.topk_weights is not None:
+        base["w"] = torch.from_numpy(ex.topk_weights).to(dev)
     sets = []
     for i in range(NB):
         s = {k: v.clone() for k, v in base.items()}
@@ -271,9 +309,16 @@ def run_ours(args, world, rank, local, pg):
 
     def fused(s):
         b = s["buf"]
-        B.moe_lora_fused_shrink_expand(s["x"], s["a"], s["b"], s["y"], b.sorted_token_ids, b.expert_ids,
-                                       b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
-                                       add_inputs=True, path=args.path, err_flag=err, stream=stream)
+        if ex is None:
+            B.moe_lora_fused_shrink_expand(s["x"], s["a0"], s["b0"], s["y"], b.sorted_token_ids, b.expert_ids,
+                                           b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
+                                           add_inputs=True, path=args.path, err_flag=err, stream=stream)
+        else:
+            B.moe_lora_fused_shrink_expand_ex(
+                s["x"], [s["a%d" % i] for i in range(args.slices)], [s["b%d" % i] for i in range(args.slices)],
+                s["y"], b.sorted_token_ids, b.expert_ids, b.num_tokens_post_padded, s["lora_ids"], w.topk,
+                w.block_size, add_inputs=True, topk_weights=s.get("w"), x_per_pair=ex.x_per_pair,
+                y_offset=ex.y_offset, path=args.path, err_flag=err, stream=stream)
 
     def step(i):
         s = sets[i % NB]
@@ -360,9 +405,11 @@ def run_ours(args, world, rank, local, pg):
         host = dict(topk_ids=torch.from_numpy(inp.topk_ids).pin_memory(),
                     mapping=torch.from_numpy(inp.token_lora_mapping).pin_memory(),
                     lora_ids=torch.from_numpy(inp.lora_ids).pin_memory(),
-                    x=torch.from_numpy(inp.x.view(np.int16)).pin_memory(),
-                    y=torch.from_numpy(inp.y_in.view(np.int16)).pin_memory())
-        out_host = torch.empty(inp.y_in.shape, dtype=torch.int16).pin_memory()
+                    x=torch.from_numpy(src.x.view(np.int16)).pin_memory(),
+                    y=torch.from_numpy(src.y_in.view(np.int16)).pin_memory())
+        if "w" in base:
+            host["w"] = torch.from_numpy(ex.topk_weights).pin_memory()
+        out_host = torch.empty(src.y_in.shape, dtype=torch.int16).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_host.numel() * out_host.element_size()
         n_e2e = max(3, min(args.steps, 2000))
@@ -375,6 +422,8 @@ def run_ours(args, world, rank, local, pg):
                 s["lora_ids"].copy_(host["lora_ids"], non_blocking=True)
                 s["x"].view(torch.int16).copy_(host["x"], non_blocking=True)
                 s["y"].view(torch.int16).copy_(host["y"], non_blocking=True)
+                if "w" in host:
+                    s["w"].copy_(host["w"], non_blocking=True)
             align(s)
             fused(s)
             with torch.cuda.stream(stream):
@@ -398,10 +447,21 @@ def run_ours(args, world, rank, local, pg):
 
     peak, peak_kind = measured_peaks()
     achieved = counts["fused_bytes"] / (fused_us * 1e-6) / 1e9
+    kernel = B.fused_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size,
+                                  args.slices, args.path)
+    kernel_name = {B.PATH_TCGEN05: "fused_tcgen05_kernel", B.PATH_CUDA_CORE_CLUSTER: "fused_cuda_core_kernel",
+                   B.PATH_CUDA_CORE_STREAM: "fused_stream_cc_kernel"}[kernel]
     return dict(ms=ms, clocks=clocks, fused_us=fused_us, align_us=align_us, counts=counts, NB=NB, l2=l2,
-                footprint=NB * per_set,
+                footprint=NB * per_set, kernel_name=kernel_name,
                 align_launches=align_launches, e2e=e2e, achieved=achieved, peak=peak, peak_kind=peak_kind,
-                inp=inp)
+                inp=inp, ex=ex)
+
+
+def ex_config(args):
+    """Config keys of the general call's options (none for the plain call)."""
+    if not uses_ex(args):
+        return {}
+    return {"num_slices": args.slices, "x_per_pair": bool(args.per_pair_x), "routed_weight": bool(args.routed_weight)}
 
 
 def main():
@@ -415,21 +475,21 @@ def main():
         rank = int(os.environ.get("RANK", "0"))
         if rank != 0:
             return
-        inp = gen.make_inputs(w)
+        inp, ex = make_step_inputs(w, args)
         # size the per-step sample so that W + K steps take a couple of minutes at most
-        probe_us, _, _ = time_oracle(inp, 0.5, 4)
+        probe_us, _, _ = time_oracle(inp, 0.5, 4, ex=ex)
         per_pair_budget = 120.0 / (args.steps + args.warmup)
         pairs_per_call = max(1, int(per_pair_budget / max(1e-9, probe_us * 1e-6 / max(1, algorithmic_counts(inp)["pairs"]))))
-        time_oracle(inp, 0, pairs_per_call, calls=args.warmup)
+        time_oracle(inp, 0, pairs_per_call, calls=args.warmup, ex=ex)
         t0 = time.perf_counter()
-        us, desc, made = time_oracle(inp, 0, pairs_per_call, calls=args.steps)
+        us, desc, made = time_oracle(inp, 0, pairs_per_call, calls=args.steps, ex=ex)
         wall = time.perf_counter() - t0
         line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/call", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded)",
-                "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "E": w.E, "topk": w.topk,
-                           "max_loras": w.max_loras, "num_active_loras": w.num_active_loras, "rank": w.rank,
-                           "block_size": w.block_size},
+                "config": dict({"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "E": w.E, "topk": w.topk,
+                                "max_loras": w.max_loras, "num_active_loras": w.num_active_loras, "rank": w.rank,
+                                "block_size": w.block_size}, **ex_config(args)),
                 "cpu_baseline": {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": desc},
                 "e2e": {"value": us, "unit": "us/call", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
                 "wall_s": wall}
@@ -446,7 +506,7 @@ def main():
     us_per_step = res["ms"] * 1e3 / (args.steps * world)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        us, desc, made = time_oracle(res["inp"], 12.0, 8)
+        us, desc, made = time_oracle(res["inp"], 12.0, 8, ex=res["ex"])
         cpu = {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": desc}
     if rank != 0:
         if pg is not None:
@@ -462,15 +522,16 @@ def main():
                    "block_size": w.block_size, "add_inputs": 1, "parallelism": "replicas" if world > 1 else "single",
                    "l2_policy": "%d rotating input sets, %.0f MB in total, L2 %.0f MB" % (
                        res["NB"], res["footprint"] / 1e6, res["l2"] / 1e6),
-                   "timing": "CUDA graphs of align+fused steps, CUDA events on the launching stream"},
+                   "timing": "CUDA graphs of align+fused steps, CUDA events on the launching stream",
+                   **ex_config(args)},
         "kernels": {"align_us": res["align_us"], "fused_us": res["fused_us"],
                     "align_launches_per_call": res["align_launches"],
                     "fused_gbs": res["achieved"],
                     "fused_tflops": counts["flops"] / (res["fused_us"] * 1e-6) / 1e12,
                     "align_gbs": counts["align_bytes"] / (res["align_us"] * 1e-6) / 1e9},
         "algorithmic": counts,
-        "roofline": {"bound": "hbm", "kernel": "fused_cuda_core_kernel" if w.M * w.topk < 1024 else
-                     "fused_tcgen05_kernel", "achieved": res["achieved"], "peak": res["peak"], "unit": "GB/s",
+        "roofline": {"bound": "hbm", "kernel": res["kernel_name"], "achieved": res["achieved"], "peak": res["peak"],
+                     "unit": "GB/s",
                      "frac": res["achieved"] / res["peak"], "peak_kind": res["peak_kind"] + " (hbm_gbs)",
                      "traffic": None},
         "cpu_baseline": cpu,

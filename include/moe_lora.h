@@ -162,7 +162,8 @@ int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping,
  *   y[f][n]   = bf16( (add_inputs ? y[f][n] : 0) + sum_j B[l][e][n][j] * t[j] )
  * t stays in registers / shared memory / tensor memory.  Pairs of slots that
  * are not listed, disabled, or not covered are not touched (in both modes).
- * Tensor-core path: t is rounded to bf16 before the second product.
+ * Tensor-core path: t enters the second product as two bf16 terms,
+ * t_hi = bf16(t) and t_lo = bf16(t - t_hi), which keeps fp32-level accuracy.
  *
  *   x                [device] bf16 [M, K] row-major
  *   lora_a           [device] bf16 [max_loras, num_experts, rank, K]
@@ -175,9 +176,11 @@ int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping,
  * Sizes: 1 <= rank <= 128 with rank % 4 == 0 (the tensor-core path needs
  * rank % 8 == 0); K % 8 == 0 and N % 8 == 0; x, lora_a, lora_b, y 16-byte
  * aligned; other limits as for moe_lora_align.  path: MOE_LORA_PATH_*; AUTO
- * picks the CUDA-core path for decode-sized batches (M*topk < 1024) and the
- * tensor-core path otherwise (when rank % 8 == 0); MOE_LORA_PATH_CUDA_CORE
- * runs the cluster kernel (MOE_LORA_PATH_CUDA_CORE_CLUSTER).
+ * picks the tensor-core path (when rank % 8 == 0) for batches of at least
+ * 1024 pairs or when the adapters the call may touch (block bound times
+ * (K + N) * rank * 2 bytes) exceed 48 MB, and the cluster kernel otherwise;
+ * MOE_LORA_PATH_CUDA_CORE runs the cluster kernel
+ * (MOE_LORA_PATH_CUDA_CORE_CLUSTER).
  */
 int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a,
                                  const moe_lora_bf16 *lora_b, moe_lora_bf16 *y,
@@ -188,6 +191,62 @@ int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lo
                                  int max_loras, int num_active_loras, int block_size,
                                  int max_num_tokens_padded, int max_num_m_blocks,
                                  int add_inputs, int path, int32_t *err_flag, void *stream);
+
+/* Most adapter slices one moe_lora_fused_shrink_expand_ex call takes. */
+#define MOE_LORA_MAX_SLICES 4
+
+/*
+ * moe_lora_fused_shrink_expand_ex -- moe_lora_fused_shrink_expand with the
+ * options the fused MoE-LoRA op carries around the same computation
+ * (mul_routed_weight / topk_weights and the output `offset` in the diff of
+ * vLLM PR #32005 to fused_moe_lora_op.py; the w13 / w2 stages of the
+ * prhub.com.cn summary of vLLM PR #42290, step 2):
+ *   - x_per_pair: x is [M*topk, K] and pair f reads row f (the w2 stage,
+ *     whose input is one activation row per pair); otherwise x is [M, K] and
+ *     pair f reads row f / topk;
+ *   - num_slices (1..MOE_LORA_MAX_SLICES) adapter slices per layer (the
+ *     separate gate and up adapters of w13): slice s has its own A_s, B_s and
+ *     rank-r intermediate t_s, and writes output columns
+ *     y_offset + s*N + n (n < N) of y rows that are ldy elements long;
+ *   - topk_weights: when not NULL, the delta of pair f is multiplied by
+ *     topk_weights[f] before it is added (mul_routed_weight):
+ *         y[f][y_offset + s*N + n] =
+ *             bf16( (add_inputs ? y_in : 0) + w[f] * sum_j B_s[l][e][n][j] * t_s[j] )
+ *     The weight scales the delta only, never y_in.
+ * Columns no slice writes are never touched.
+ *
+ *   x                [device] bf16 [M, K], or [M*topk, K] when x_per_pair
+ *   lora_a, lora_b   [host] arrays of num_slices [device] pointers, each as in
+ *                    moe_lora_fused_shrink_expand (same shapes for every slice);
+ *                    the host arrays are read during the call only
+ *   y                [device] bf16 [M, topk, ldy]
+ *   topk_weights     [device] fp32 [M, topk], or NULL
+ * Sizes: ldy % 8 == 0, y_offset % 8 == 0, y_offset + num_slices*N <= ldy;
+ * the rest as for moe_lora_fused_shrink_expand, which is this call with
+ * x_per_pair = 0, one slice, ldy = N, y_offset = 0 and no weights.
+ */
+int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair,
+                                    const moe_lora_bf16 *const *lora_a,
+                                    const moe_lora_bf16 *const *lora_b, int num_slices,
+                                    moe_lora_bf16 *y, int ldy, int y_offset,
+                                    const float *topk_weights,
+                                    const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                                    const int32_t *num_tokens_post_padded,
+                                    const int32_t *lora_ids, const int32_t *adapter_enabled,
+                                    int M, int topk, int num_experts, int K, int N, int rank,
+                                    int max_loras, int num_active_loras, int block_size,
+                                    int max_num_tokens_padded, int max_num_m_blocks,
+                                    int add_inputs, int path, int32_t *err_flag, void *stream);
+
+/*
+ * moe_lora_fused_resolve_path -- the kernel a fused call with these sizes
+ * runs: MOE_LORA_PATH_TCGEN05, MOE_LORA_PATH_CUDA_CORE_CLUSTER or
+ * MOE_LORA_PATH_CUDA_CORE_STREAM (never AUTO or CUDA_CORE), or a negative
+ * moe_lora_status code if `path` is not valid for these sizes.  Host only; no
+ * device is touched.
+ */
+int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank,
+                                int num_active_loras, int block_size, int num_slices, int path);
 
 /* Size of the scratch buffer built into the library for
  * moe_lora_align_static_workspace (4 MiB). */

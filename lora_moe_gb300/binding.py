@@ -62,6 +62,12 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_fused_shrink_expand.restype = I
             L.moe_lora_fused_shrink_expand.argtypes = [P, P, P, P, P, P, P, P, P,
                                                        I, I, I, I, I, I, I, I, I, I, I, I, I, P, P]
+            L.moe_lora_fused_shrink_expand_ex.restype = I
+            L.moe_lora_fused_shrink_expand_ex.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P), I, P, I, I, P,
+                                                          P, P, P, P, P,
+                                                          I, I, I, I, I, I, I, I, I, I, I, I, I, P, P]
+            L.moe_lora_fused_resolve_path.restype = I
+            L.moe_lora_fused_resolve_path.argtypes = [I] * 10
             _lib = L
     return _lib
 
@@ -165,6 +171,60 @@ def moe_lora_fused_shrink_expand(x, lora_a, lora_b, y, sorted_token_ids, expert_
         sorted_token_ids.shape[-1], expert_ids.shape[-1], int(bool(add_inputs)), path,
         _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
     _check(st, "moe_lora_fused_shrink_expand")
+
+
+def fused_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices=1,
+                       path=PATH_AUTO) -> int:
+    """The kernel a fused call with these sizes runs (PATH_TCGEN05,
+    PATH_CUDA_CORE_CLUSTER or PATH_CUDA_CORE_STREAM)."""
+    v = lib().moe_lora_fused_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, block_size,
+                                          num_slices, path)
+    if v < 0:
+        raise MoeLoraError(-v, "moe_lora_fused_resolve_path")
+    return v
+
+
+def moe_lora_fused_shrink_expand_ex(x, lora_a, lora_b, y, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                                    lora_ids, topk, block_size, add_inputs=True, adapter_enabled=None,
+                                    topk_weights=None, x_per_pair=False, y_offset=0,
+                                    path=PATH_AUTO, err_flag=None, stream=None):
+    """moe_lora_fused_shrink_expand_ex on device tensors; y is updated in place.
+
+    lora_a / lora_b: a tensor (one slice) or a list of per-slice tensors
+    ([L, E, r, K] / [L, E, N, r]).  x: [M, K], or [M*topk, K] with x_per_pair.
+    y: [M, topk, ldy]; slice s writes columns y_offset + s*N .. + N.
+    topk_weights: float32 [M, topk] or None."""
+    if isinstance(lora_a, torch.Tensor):
+        lora_a, lora_b = [lora_a], [lora_b]
+    S = len(lora_a)
+    if S < 1 or len(lora_b) != S:
+        raise ValueError("lora_a and lora_b need the same number of slices")
+    L, E, r, K = lora_a[0].shape
+    N = lora_b[0].shape[2]
+    for a, b in zip(lora_a, lora_b):
+        if tuple(a.shape) != (L, E, r, K) or tuple(b.shape) != (L, E, N, r):
+            raise ValueError("inconsistent slice shapes")
+    if y.dim() != 3:
+        raise ValueError("y must be [M, topk, ldy]")
+    M = y.shape[0]
+    ldy = y.shape[2]
+    if y.shape[1] != topk or tuple(x.shape) != ((M * topk if x_per_pair else M), K):
+        raise ValueError("inconsistent shapes")
+    if topk_weights is not None and topk_weights.numel() != M * topk:
+        raise ValueError("topk_weights must be [M, topk]")
+    bf = torch.bfloat16
+    a_ptrs = (ctypes.c_void_p * S)(*[_ptr(a, bf, "lora_a") for a in lora_a])
+    b_ptrs = (ctypes.c_void_p * S)(*[_ptr(b, bf, "lora_b") for b in lora_b])
+    st = lib().moe_lora_fused_shrink_expand_ex(
+        _ptr(x, bf, "x"), int(bool(x_per_pair)), a_ptrs, b_ptrs, S, _ptr(y, bf, "y"), ldy, y_offset,
+        _ptr(topk_weights, torch.float32, "topk_weights"),
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(num_tokens_post_padded, torch.int32, "num_tokens_post_padded"),
+        _ptr(lora_ids, torch.int32, "lora_ids"), _ptr(adapter_enabled, torch.int32, "adapter_enabled"),
+        M, topk, E, K, N, r, L, lora_ids.numel(), block_size,
+        sorted_token_ids.shape[-1], expert_ids.shape[-1], int(bool(add_inputs)), path,
+        _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+    _check(st, "moe_lora_fused_shrink_expand_ex")
 
 
 class AlignBuffers:

@@ -79,6 +79,25 @@ int resolve_align_variant(int M, int topk, int E, int variant) {
 
 }  // namespace
 
+// The kernel a fused call runs.  AUTO takes the tensor-core kernel (when it
+// supports the sizes) for batches of at least 1024 pairs or when the adapter
+// bytes the call may touch, by the block bound, exceed 48 MB: there the
+// balanced persistent tile ranges keep every SM streaming.  Otherwise, and for
+// MOE_LORA_PATH_CUDA_CORE, the cluster kernel: on every decode workload
+// measured it beat the streaming CUDA-core kernel, which recomputes the shrink
+// of a block in every CTA whose tile range touches it.
+static int resolve_path(const FusedArgs &f, int path) {
+  int use = path;
+  if (use == MOE_LORA_PATH_AUTO) {
+    const double touched = (double)fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size) *
+                           f.num_slices * (double)(f.K + f.N) * f.rank * 2.0;
+    const bool big = (long long)f.M * f.topk >= 1024 || touched > 48.0e6;
+    use = (big && tcgen05_path_supports(f)) ? MOE_LORA_PATH_TCGEN05 : MOE_LORA_PATH_CUDA_CORE;
+  }
+  if (use == MOE_LORA_PATH_CUDA_CORE) use = MOE_LORA_PATH_CUDA_CORE_CLUSTER;
+  return use;
+}
+
 extern "C" {
 
 int moe_lora_version(void) { return 100; }
@@ -158,33 +177,65 @@ int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping, c
   return launch_align_global(a, workspace, s);
 }
 
-int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a, const moe_lora_bf16 *lora_b,
-                                 moe_lora_bf16 *y, const int32_t *sorted_token_ids, const int32_t *expert_ids,
-                                 const int32_t *num_tokens_post_padded, const int32_t *lora_ids,
-                                 const int32_t *adapter_enabled, int M, int topk, int num_experts, int K, int N,
-                                 int rank, int max_loras, int num_active_loras, int block_size,
-                                 int max_num_tokens_padded, int max_num_m_blocks, int add_inputs, int path,
-                                 int32_t *err_flag, void *stream) {
+int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
+                                int block_size, int num_slices, int path) {
+  if (M < 0 || topk < 1 || num_experts < 1 || K < 8 || N < 8 || rank < 1 || num_active_loras < 0 ||
+      num_slices < 1 || num_slices > kMaxSlices || path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_CUDA_CORE_STREAM)
+    return -MOE_LORA_ERR_INVALID_ARG;
+  if (!valid_block_size(block_size) || rank > kMaxRank || rank % 4 != 0) return -MOE_LORA_ERR_UNSUPPORTED;
+  if ((path == MOE_LORA_PATH_TCGEN05 || path == MOE_LORA_PATH_CUDA_CORE_STREAM) && rank % 8 != 0)
+    return -MOE_LORA_ERR_UNSUPPORTED;
+  FusedArgs f = {};
+  f.M = M;
+  f.topk = topk;
+  f.num_experts = num_experts;
+  f.K = K;
+  f.N = N;
+  f.rank = rank;
+  f.num_active_loras = num_active_loras;
+  f.block_size = block_size;
+  f.num_slices = num_slices;
+  return resolve_path(f, path);
+}
+
+int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair, const moe_lora_bf16 *const *lora_a,
+                                    const moe_lora_bf16 *const *lora_b, int num_slices, moe_lora_bf16 *y, int ldy,
+                                    int y_offset, const float *topk_weights, const int32_t *sorted_token_ids,
+                                    const int32_t *expert_ids, const int32_t *num_tokens_post_padded,
+                                    const int32_t *lora_ids, const int32_t *adapter_enabled, int M, int topk,
+                                    int num_experts, int K, int N, int rank, int max_loras, int num_active_loras,
+                                    int block_size, int max_num_tokens_padded, int max_num_m_blocks, int add_inputs,
+                                    int path, int32_t *err_flag, void *stream) {
   if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
                             max_num_m_blocks))
     return st;
   if (K < 8 || N < 8 || rank < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_slices < 1 || num_slices > kMaxSlices || !lora_a || !lora_b) return MOE_LORA_ERR_INVALID_ARG;
+  if (y_offset < 0 || ldy < 8 || (long long)y_offset + (long long)num_slices * N > ldy) return MOE_LORA_ERR_INVALID_ARG;
   if (rank > kMaxRank || rank % 4 != 0) return MOE_LORA_ERR_UNSUPPORTED;
-  if (K % 8 != 0 || N % 8 != 0) return MOE_LORA_ERR_MISALIGNED;
+  if (K % 8 != 0 || N % 8 != 0 || ldy % 8 != 0 || y_offset % 8 != 0) return MOE_LORA_ERR_MISALIGNED;
   if (path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_CUDA_CORE_STREAM) return MOE_LORA_ERR_INVALID_ARG;
   if ((path == MOE_LORA_PATH_TCGEN05 || path == MOE_LORA_PATH_CUDA_CORE_STREAM) && rank % 8 != 0)
     return MOE_LORA_ERR_UNSUPPORTED;
-  if ((long long)M * K > INT32_MAX * 8LL || (long long)M * topk * N > INT32_MAX * 8LL)
-    return MOE_LORA_ERR_UNSUPPORTED;
+  const long long x_rows = x_per_pair ? (long long)M * topk : (long long)M;
+  if (x_rows * K > INT32_MAX * 8LL || (long long)M * topk * ldy > INT32_MAX * 8LL) return MOE_LORA_ERR_UNSUPPORTED;
   if (num_active_loras == 0 || M == 0) return MOE_LORA_OK;
-  if (!x || !lora_a || !lora_b || !y || !sorted_token_ids || !expert_ids || !num_tokens_post_padded || !lora_ids)
+  if (!x || !y || !sorted_token_ids || !expert_ids || !num_tokens_post_padded || !lora_ids)
     return MOE_LORA_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(lora_a) || !aligned16(lora_b) || !aligned16(y)) return MOE_LORA_ERR_MISALIGNED;
+  for (int s = 0; s < num_slices; ++s) {
+    if (!lora_a[s] || !lora_b[s]) return MOE_LORA_ERR_INVALID_ARG;
+    if (!aligned16(lora_a[s]) || !aligned16(lora_b[s])) return MOE_LORA_ERR_MISALIGNED;
+  }
+  if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
+    return MOE_LORA_ERR_MISALIGNED;
   FusedArgs f;
   f.x = x;
-  f.lora_a = lora_a;
-  f.lora_b = lora_b;
+  for (int s = 0; s < kMaxSlices; ++s) {
+    f.lora_a[s] = lora_a[s < num_slices ? s : 0];
+    f.lora_b[s] = lora_b[s < num_slices ? s : 0];
+  }
   f.y = y;
+  f.topk_weights = topk_weights;
   f.sorted_token_ids = sorted_token_ids;
   f.expert_ids = expert_ids;
   f.num_tokens_post_padded = num_tokens_post_padded;
@@ -203,20 +254,32 @@ int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lo
   f.max_num_tokens_padded = max_num_tokens_padded;
   f.max_num_m_blocks = max_num_m_blocks;
   f.add_inputs = add_inputs ? 1 : 0;
-  int use = path;
-  if (use == MOE_LORA_PATH_AUTO)
-    use = ((long long)M * topk >= 1024 && tcgen05_path_supports(f)) ? MOE_LORA_PATH_TCGEN05
-                                                                     : MOE_LORA_PATH_CUDA_CORE;
-  // On every decode workload measured, the cluster kernel beat the streaming
-  // one (the streaming kernel recomputes the shrink of a block in every CTA
-  // whose tile range touches it), so the CUDA-core choice is the cluster kernel.
-  if (use == MOE_LORA_PATH_CUDA_CORE) use = MOE_LORA_PATH_CUDA_CORE_CLUSTER;
+  f.num_slices = num_slices;
+  f.x_per_pair = x_per_pair ? 1 : 0;
+  f.ldy = ldy;
+  f.y_offset = y_offset;
+  const int use = resolve_path(f, path);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (use) {
     case MOE_LORA_PATH_TCGEN05: return launch_fused_tcgen05(f, s);
     case MOE_LORA_PATH_CUDA_CORE_STREAM: return launch_fused_stream_cc(f, s);
     default: return launch_fused_cuda_core(f, s);
   }
+}
+
+int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a, const moe_lora_bf16 *lora_b,
+                                 moe_lora_bf16 *y, const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                                 const int32_t *num_tokens_post_padded, const int32_t *lora_ids,
+                                 const int32_t *adapter_enabled, int M, int topk, int num_experts, int K, int N,
+                                 int rank, int max_loras, int num_active_loras, int block_size,
+                                 int max_num_tokens_padded, int max_num_m_blocks, int add_inputs, int path,
+                                 int32_t *err_flag, void *stream) {
+  const moe_lora_bf16 *a[1] = {lora_a};
+  const moe_lora_bf16 *b[1] = {lora_b};
+  return moe_lora_fused_shrink_expand_ex(x, 0, a, b, 1, y, N, 0, nullptr, sorted_token_ids, expert_ids,
+                                         num_tokens_post_padded, lora_ids, adapter_enabled, M, topk, num_experts, K,
+                                         N, rank, max_loras, num_active_loras, block_size, max_num_tokens_padded,
+                                         max_num_m_blocks, add_inputs, path, err_flag, stream);
 }
 
 }  // extern "C"

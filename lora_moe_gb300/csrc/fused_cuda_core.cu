@@ -2,9 +2,11 @@
 // cores (sm_103a).
 //
 // Computes, for every block b of every active slot z (l = lora_ids[z],
-// e = expert_ids[l][b]) and every pair f of that block (m = f / topk):
-//     t[j]    = sum_k x[m][k] * A[l][e][j][k]                 (fp32)
-//     y[f][n] = bf16((add_inputs ? y[f][n] : 0) + sum_j B[l][e][n][j] * t[j])
+// e = expert_ids[l][b]), every adapter slice s and every pair f of that block
+// (input row x_f: row f / topk, or row f when x holds one row per pair; router
+// weight w_f, 1 without weights):
+//     t[j]    = sum_k x_f[k] * A_s[l][e][j][k]                (fp32)
+//     y[f][off + s*N + n] = bf16((add_inputs ? y_in : 0) + w_f * sum_j B_s[l][e][n][j] * t[j])
 // (prhub.com.cn summary of vLLM PR #42290, "Implementation breakdown" step 1:
 // one kernel does the shrink by lora_a and the expand by lora_b and keeps the
 // rank dimension on chip; its small-batch kernel is the decode specialisation.)
@@ -12,9 +14,10 @@
 // At decode sizes a block holds one or two real pairs, so the work is a skinny
 // GEMV bound by reading A[l,e] (r x K) and B[l,e] (N x r) -- and, at a few
 // megabytes per call, by latency.  Design:
-//   * grid (C, num_active_loras, blocks): CTA (c, z, b) serves block b of slot z
-//     (vLLM PR #32005: the LoRA grid dimension is the number of active LoRAs);
-//     blocks past num_tokens_post_padded exit after one dependent load.
+//   * grid (C, num_slices * num_active_loras, blocks): CTA (c, s * nact + z, b)
+//     serves slice s of block b of slot z (vLLM PR #32005: the LoRA grid
+//     dimension is the number of active LoRAs); blocks past
+//     num_tokens_post_padded exit after one dependent load.
 //   * a thread-block cluster of C CTAs shares a block: CTA c streams the
 //     K-slice c of A and of the gathered x rows and the N-slice c of B and y;
 //     the C partial t's are summed through distributed shared memory in rank
@@ -53,7 +56,8 @@ struct CcCfg {
 struct Meta {
   uint64_t bar;                  // the B slice's bulk copy
   int pf[kMaxBlock];             // the block's real pairs (flat index), in order
-  int pm[kMaxBlock];             // their token index
+  int pm[kMaxBlock];             // their row of x
+  float pw[kMaxBlock];           // their router weight
   int wcount[kWarps];
   int nv;
   int abort;
@@ -101,12 +105,13 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = p.rank, K = p.K, N = p.N, E = p.num_experts, bs = p.block_size;
   const int P = p.M * p.topk;
-  const int z = blockIdx.y;
+  const int z = blockIdx.y % p.num_active_loras;
+  const int sl = blockIdx.y / p.num_active_loras;   // adapter slice
 
   // Uniform over the cluster: every CTA of it reads the same values.
   const int l = __ldg(p.lora_ids + z);
   if (l < 0 || l >= p.max_loras) {
-    if (c == 0 && tid == 0 && blockIdx.z == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
+    if (c == 0 && tid == 0 && blockIdx.z == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
     return;
   }
   if (p.adapter_enabled && __ldg(p.adapter_enabled + l) == 0) return;
@@ -145,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
       if (tid < bs && idx < p.max_num_tokens_padded) {
         f = b == b_first ? f_first : __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + idx);
         if (f < 0 || f > P) {
-          if (c == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
+          if (c == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
           f = -1;
         } else if (f == P) {
           f = -1;
@@ -163,19 +168,20 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
       if (f >= 0) {
         const int pos = base + __popc(bal & ((1u << lane) - 1u));
         meta.pf[pos] = f;
-        meta.pm[pos] = f / p.topk;
+        meta.pm[pos] = x_row(p, f);
+        meta.pw[pos] = route_weight(p, f);
       }
       if (tid == 0) meta.nv = tot;
       __syncthreads();
     }
     if (e < 0 || e >= E) {  // uniform over the cluster
-      if (tid == 0 && c == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
+      if (tid == 0 && c == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
       continue;
     }
     const int nv = meta.nv;
     const size_t le = (size_t)l * E + e;
-    const uint16_t *A = p.lora_a + le * r * K;
-    const uint16_t *Bm = p.lora_b + le * N * r;
+    const uint16_t *A = slice_a(p, sl) + le * r * K;
+    const uint16_t *Bm = slice_b(p, sl) + le * N * r;
 
     for (int g0 = 0; g0 < nv; g0 += kPG) {
       const int nvg = min(kPG, nv - g0);
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
           for (int i = tid; i < nvg * nch; i += kThreads) {
             const int q = i / nch, ch = i - q * nch;
             cp_async_16(y_s + (size_t)q * cfg.nslice * 2 + ch * 16,
-                        p.y + (size_t)meta.pf[g0 + q] * N + n_lo + ch * 8, 16u);
+                        p.y + y_base(p, meta.pf[g0 + q], sl) + n_lo + ch * 8, 16u);
           }
         cp_async_commit();
       }
@@ -300,7 +306,7 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
                                       ? bf16_bits_to_float(reinterpret_cast<const uint16_t *>(
                                             y_s + (size_t)q * cfg.nslice * 2)[nl])
                                       : 0.f;
-                p.y[(size_t)meta.pf[g0 + q] * N + n_lo + nl] = float_to_bf16_bits(v + old);
+                p.y[y_base(p, meta.pf[g0 + q], sl) + n_lo + nl] = float_to_bf16_bits(v * meta.pw[g0 + q] + old);
               }
             }
           }
@@ -364,7 +370,7 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = current_device_info(&dev)) return st;
   if (f.block_size > kMaxBlock) return MOE_LORA_ERR_UNSUPPORTED;
-  if (f.num_active_loras > 65535) return MOE_LORA_ERR_UNSUPPORTED;
+  if ((long long)f.num_active_loras * f.num_slices > 65535) return MOE_LORA_ERR_UNSUPPORTED;
   CcCfg cfg;
   if (int st = pick_cfg(f, dev, &cfg)) return st;
   // Blocks one slot can produce: floor(M*topk / bs) full ones plus one partly
@@ -374,7 +380,8 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   if (per_slot > f.max_num_m_blocks) per_slot = f.max_num_m_blocks;
   // Blocks a slot really has are usually far fewer than that bound; past a few
   // waves of clusters, CTAs walk several blocks instead of launching empty.
-  const long long cap = std::max<long long>(48, 4LL * dev.sm_count / ((long long)cfg.C * f.num_active_loras));
+  const long long cap =
+      std::max<long long>(48, 4LL * dev.sm_count / ((long long)cfg.C * f.num_active_loras * f.num_slices));
   if (per_slot > cap) per_slot = cap;
   if (per_slot > 65535) per_slot = 65535;
   if (per_slot <= 0) return 0;
@@ -385,7 +392,7 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   if (cfg.C > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
     return MOE_LORA_ERR_LAUNCH;
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(cfg.C, f.num_active_loras, (unsigned)per_slot);
+  lc.gridDim = dim3(cfg.C, f.num_active_loras * f.num_slices, (unsigned)per_slot);
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = cfg.smem_bytes;
   lc.stream = stream;

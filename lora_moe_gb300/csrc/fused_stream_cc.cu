@@ -1,10 +1,11 @@
 // fused_stream_cc.cu -- the fused MoE-LoRA shrink+expand on CUDA cores for
 // decode-sized blocks with large adapters (sm_103a).
 //
-// Computes, for each block of each listed slot (l, e) and each real pair f of
-// the block (m = f / topk):
-//     t[j]    = sum_k x[m][k] * A[l][e][j][k]                 (fp32)
-//     y[f][n] = bf16((add_inputs ? y[f][n] : 0) + sum_j B[l][e][n][j] * t[j])
+// Computes, for each block of each listed slot (l, e), each adapter slice s
+// and each real pair f of the block (input row x_f: row f / topk, or row f
+// when x holds one row per pair; router weight w_f, 1 without weights):
+//     t[j]    = sum_k x_f[k] * A_s[l][e][j][k]                (fp32)
+//     y[f][off + s*N + n] = bf16((add_inputs ? y_in : 0) + w_f * sum_j B_s[l][e][n][j] * t[j])
 // (prhub.com.cn summary of vLLM PR #42290, "Implementation breakdown" step 1;
 // its small-batch kernel is the decode specialisation of the one-shot kernel.)
 //
@@ -52,8 +53,7 @@ __device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b) {
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
-    fused_stream_cc_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                           const FusedArgs p, const stream::Cfg cfg) {
+    fused_stream_cc_kernel(const __grid_constant__ stream::TmapSet maps, const FusedArgs p, const stream::Cfg cfg) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   stream::Meta &meta = *reinterpret_cast<stream::Meta *>(smem + cfg.off_meta);
@@ -74,19 +74,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     meta.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensor_map(&tmap_a);
-    prefetch_tensor_map(&tmap_b);
+  if (warp == 0 && lane < p.num_slices) {
+    prefetch_tensor_map(&maps.a[lane]);
+    prefetch_tensor_map(&maps.b[lane]);
   }
   wait_for_prior_grid();   // align outputs are read from here on
   stream::slot_prefix<BS>(p, meta);
   __syncthreads();
-  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, cfg.nt_total);
+  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, p.num_slices, cfg.nt_total);
 
   if (warp == 9 || warp == 10) {
-    stream::shrink_producer<BS>(p, cfg, meta, &tmap_a, sh_base, rg, warp - 9);
+    stream::shrink_producer<BS>(p, cfg, meta, &maps, sh_base, rg, warp - 9);
   } else if (warp == 0) {
-    stream::expand_producer<BS>(p, cfg, meta, &tmap_b, ex_base, rg);
+    stream::expand_producer<BS>(p, cfg, meta, &maps, ex_base, rg);
   } else {
     const int ctid = tid - 32, cwarp = warp - 1;
     const int N = p.N, E = p.num_experts, r = p.rank, r_pad = cfg.r_pad, P = p.M * p.topk;
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ctid < BS) {
         f = __ldg(br.ids + ctid);
         valid = f >= 0 && f < P && e_ok;
-        if (f < 0 || f > P) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
+        if ((f < 0 || f > P) && br.s == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
       }
       const unsigned bal = __ballot_sync(0xffffffffu, valid);
       if (lane == 0) meta.wcount[cwarp] = __popc(bal);
@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pos = base + __popc(bal & ((1u << lane) - 1u));
         meta.cpx[pos] = ctid;
         meta.epi_f[pos] = f;
+        meta.epi_w[pos] = route_weight(p, f);
       }
       named_barrier(1, kCompThreads);
 
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (n0 + n < N) {
             uint16_t *dst = reinterpret_cast<uint16_t *>(yt + meta.cpx[pi] * (stream::kTileN * 2)) + n;
+            a *= meta.epi_w[pi];
             if (p.add_inputs) a += bf16_bits_to_float(*dst);
             *dst = float_to_bf16_bits(a);
           }
@@ -197,7 +199,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int pi = item >> 4, c16 = item & 15;
           const int nn = n0 + c16 * 8;
           if (nn < N)
-            *reinterpret_cast<uint4 *>(p.y + (size_t)meta.epi_f[pi] * N + nn) =
+            *reinterpret_cast<uint4 *>(p.y + y_base(p, meta.epi_f[pi], br.s) + nn) =
                 *reinterpret_cast<const uint4 *>(yt + meta.cpx[pi] * (stream::kTileN * 2) + c16 * 16);
         }
         __syncwarp();
@@ -208,8 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BS>
-int launch_bs(const FusedArgs &f, const stream::Cfg &cfg, const CUtensorMap &ta, const CUtensorMap &tb, int G,
-              cudaStream_t s) {
+int launch_bs(const FusedArgs &f, const stream::Cfg &cfg, const stream::TmapSet &maps, int G, cudaStream_t s) {
   const void *fn = (const void *)fused_stream_cc_kernel<BS>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes) != cudaSuccess)
     return MOE_LORA_ERR_LAUNCH;
@@ -225,7 +226,7 @@ int launch_bs(const FusedArgs &f, const stream::Cfg &cfg, const CUtensorMap &ta,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  const cudaError_t err = cudaLaunchKernelEx(&lc, fused_stream_cc_kernel<BS>, ta, tb, f, cfg);
+  const cudaError_t err = cudaLaunchKernelEx(&lc, fused_stream_cc_kernel<BS>, maps, f, cfg);
   return err == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
 }
 
@@ -244,19 +245,19 @@ int launch_fused_stream_cc(const FusedArgs &f, cudaStream_t s) {
   const int r_pad = r16 <= 16 ? 16 : (r16 <= 32 ? 32 : (r16 <= 64 ? 64 : 128));
   stream::Cfg cfg;
   if (int st = stream::plan(f, dev, f.block_size * r_pad * 4, 1, &cfg)) return st;
-  CUtensorMap ta, tb;
-  if (int st = stream::make_tensor_maps(f, cfg, &ta, &tb)) return st;
+  stream::TmapSet maps;
+  if (int st = stream::make_tensor_maps(f, cfg, &maps)) return st;
   const long long bound = fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size);
   if (bound <= 0) return 0;
   const int per_sm = std::max(1, (228 * 1024) / (cfg.smem_bytes + 1024));
   long long G = (long long)dev.sm_count * per_sm;
-  if (G > bound * cfg.nt_total) G = bound * cfg.nt_total;
+  if (G > bound * f.num_slices * cfg.nt_total) G = bound * f.num_slices * cfg.nt_total;
   if (G < 1) G = 1;
   switch (f.block_size) {
-    case 16: return launch_bs<16>(f, cfg, ta, tb, (int)G, s);
-    case 32: return launch_bs<32>(f, cfg, ta, tb, (int)G, s);
-    case 64: return launch_bs<64>(f, cfg, ta, tb, (int)G, s);
-    case 128: return launch_bs<128>(f, cfg, ta, tb, (int)G, s);
+    case 16: return launch_bs<16>(f, cfg, maps, (int)G, s);
+    case 32: return launch_bs<32>(f, cfg, maps, (int)G, s);
+    case 64: return launch_bs<64>(f, cfg, maps, (int)G, s);
+    case 128: return launch_bs<128>(f, cfg, maps, (int)G, s);
     default: return MOE_LORA_ERR_UNSUPPORTED;
   }
 }

@@ -3,16 +3,18 @@
 //
 // Same definition as the CUDA-core path (prhub.com.cn summary of vLLM PR
 // #42290, "Implementation breakdown" step 1: shrink by lora_a, expand by
-// lora_b, rank dimension kept on chip, add_inputs accumulate/overwrite):
-//     T[p][j]   = sum_k x[m_p][k] * A[l][e][j][k]        p < block_size, j < r
-//     y[f_p][n] = bf16((add ? y[f_p][n] : 0) + sum_j B[l][e][n][j] * T[p][j])
+// lora_b, rank dimension kept on chip, add_inputs accumulate/overwrite), per
+// adapter slice s, with the pair's input row x_p (row m or row f) and router
+// weight w_p (1 without weights):
+//     T[p][j]   = sum_k x_p[k] * A_s[l][e][j][k]           p < block_size, j < r
+//     y[f_p][off + s*N + n] = bf16((add ? y_in : 0) + w_p * sum_j B_s[l][e][n][j] * T[p][j])
 //
-// Work split.  The work of a call is the list of (block, 128-column tile)
-// pairs over all blocks of all listed slots (vLLM PR #32005: the grid is sized
-// by the active LoRAs).  Each persistent CTA takes one contiguous, equal share
-// of that list, so every SM streams the same number of output tiles; a block
-// whose tiles straddle two CTAs has its shrink computed by both.  T lives only
-// in shared and tensor memory.
+// Work split.  The work of a call is the list of (unit, 128-column tile)
+// pairs, a unit being one adapter slice of one block of a listed slot (vLLM
+// PR #32005: the grid is sized by the active LoRAs).  Each persistent CTA takes
+// one contiguous, equal share of that list, so every SM streams the same
+// number of output tiles; a unit whose tiles straddle two CTAs has its shrink
+// computed by both.  T lives only in shared and tensor memory.
 //
 // Warp roles (416 threads):
 //   warps 10, 11  shrink producers: alternate k-tiles; gather the block's x rows
@@ -53,8 +55,7 @@ constexpr int kMmaRows = 128;     // M of every tcgen05.mma here
 
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
-    fused_tcgen05_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                         const FusedArgs p, const stream::Cfg cfg) {
+    fused_tcgen05_kernel(const __grid_constant__ stream::TmapSet maps, const FusedArgs p, const stream::Cfg cfg) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   stream::Meta &meta = *reinterpret_cast<stream::Meta *>(smem + cfg.off_meta);
@@ -89,9 +90,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     meta.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensor_map(&tmap_a);
-    prefetch_tensor_map(&tmap_b);
+  if (warp == 0 && lane < p.num_slices) {
+    prefetch_tensor_map(&maps.a[lane]);
+    prefetch_tensor_map(&maps.b[lane]);
   }
   if (warp == 1) {
     tmem_alloc(&meta.tmem_base, cfg.tmem_cols);
@@ -105,13 +106,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = meta.tmem_base;
   const uint32_t tmem_sh = tmem + cfg.nacc * BS;   // shrink accumulator columns
 
-  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, nt_total);
+  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, p.num_slices, nt_total);
   const int gb0 = rg.gb0, gb1 = rg.gb1;
   auto tile_lo = [&](int gb) { return rg.tile_lo(gb); };
   auto tile_hi = [&](int gb) { return rg.tile_hi(gb); };
 
   if (warp == 10 || warp == 11) {
-    stream::shrink_producer<BS>(p, cfg, meta, &tmap_a, sh_base, rg, warp - 10);
+    stream::shrink_producer<BS>(p, cfg, meta, &maps, sh_base, rg, warp - 10);
   } else if (warp == 12) {
     // ======================= shrink MMA issuer
     if (lane == 0) {
@@ -138,7 +139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 0) {
-    stream::expand_producer<BS>(p, cfg, meta, &tmap_b, ex_base, rg);
+    stream::expand_producer<BS>(p, cfg, meta, &maps, ex_base, rg);
   } else if (warp == 1) {
     // ======================= expand MMA issuer
     if (lane == 0) {
@@ -194,8 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int f = __ldg(br.ids + etid);
         int v = -1;
         if (f >= 0 && f < P && e_ok) v = f;
-        else if (f < 0 || f > P) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
+        else if ((f < 0 || f > P) && br.s == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
         meta.epi_f[etid] = v;
+        meta.epi_w[etid] = v >= 0 ? route_weight(p, v) : 0.f;
       }
       named_barrier(1, kEpiThreads);
       uint32_t valid[kChunks];   // bit i of valid[c]: row kCR*c + i is a real pair
@@ -205,6 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < kCR; ++i) valid[c] |= (uint32_t)(meta.epi_f[kCR * c + i] >= 0) << i;
       }
+      const bool weighted = p.topk_weights != nullptr;
+      const size_t s_col = (size_t)p.y_offset + (size_t)br.s * N;   // the slice's first output column
       int st_f[kStoreRows];
 #pragma unroll
       for (int i = 0; i < kStoreRows; ++i) st_f[i] = meta.epi_f[(gtid >> 4) + 8 * i];
@@ -278,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_wait_ld();
           if (col_ok) {
+            if (weighted) {
+#pragma unroll
+              for (int i = 0; i < kCR; ++i) v[i] *= meta.epi_w[kCR * c + i];
+            }
             if (p.add_inputs) {
               uint16_t old[kCR];   // all loads first, then all stores
 #pragma unroll
@@ -306,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               vals[i] = *reinterpret_cast<const uint4 *>(yt + ((gtid >> 4) + 8 * i) * (stream::kTileN * 2) + c16 * 16);
 #pragma unroll
             for (int i = 0; i < kStoreRows; ++i)
-              if (st_f[i] >= 0) *reinterpret_cast<uint4 *>(p.y + (size_t)st_f[i] * N + nn) = vals[i];
+              if (st_f[i] >= 0) *reinterpret_cast<uint4 *>(p.y + (size_t)st_f[i] * p.ldy + s_col + nn) = vals[i];
           }
         }
         __syncwarp();
@@ -324,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BS>
-int launch_bs(const FusedArgs &f, const stream::Cfg &cfg, const CUtensorMap &ta, const CUtensorMap &tb, int G,
+int launch_bs(const FusedArgs &f, const stream::Cfg &cfg, const stream::TmapSet &maps, int G,
               cudaStream_t stream) {
   const void *fn = (const void *)fused_tcgen05_kernel<BS>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes) != cudaSuccess)
@@ -341,7 +349,7 @@ int launch_bs(const FusedArgs &f, const stream::Cfg &cfg, const CUtensorMap &ta,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  const cudaError_t err = cudaLaunchKernelEx(&lc, fused_tcgen05_kernel<BS>, ta, tb, f, cfg);
+  const cudaError_t err = cudaLaunchKernelEx(&lc, fused_tcgen05_kernel<BS>, maps, f, cfg);
   return err == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
 }
 
@@ -371,19 +379,19 @@ int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream_) {
   // memory that they never need more than that.
   while (((228 * 1024) / (cfg.smem_bytes + 1024)) * cols > 512) cfg.smem_bytes += 4096;
   if (cfg.smem_bytes > (int)dev.max_smem_optin) return MOE_LORA_ERR_UNSUPPORTED;
-  CUtensorMap ta, tb;
-  if (int st = stream::make_tensor_maps(f, cfg, &ta, &tb)) return st;
+  stream::TmapSet maps;
+  if (int st = stream::make_tensor_maps(f, cfg, &maps)) return st;
   const long long bound = fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size);
   if (bound <= 0) return 0;
   const int per_sm = std::max(1, (228 * 1024) / (cfg.smem_bytes + 1024));
   long long G = (long long)dev.sm_count * per_sm;
-  if (G > bound * cfg.nt_total) G = bound * cfg.nt_total;
+  if (G > bound * f.num_slices * cfg.nt_total) G = bound * f.num_slices * cfg.nt_total;
   if (G < 1) G = 1;
   switch (f.block_size) {
-    case 16: return launch_bs<16>(f, cfg, ta, tb, (int)G, stream_);
-    case 32: return launch_bs<32>(f, cfg, ta, tb, (int)G, stream_);
-    case 64: return launch_bs<64>(f, cfg, ta, tb, (int)G, stream_);
-    case 128: return launch_bs<128>(f, cfg, ta, tb, (int)G, stream_);
+    case 16: return launch_bs<16>(f, cfg, maps, (int)G, stream_);
+    case 32: return launch_bs<32>(f, cfg, maps, (int)G, stream_);
+    case 64: return launch_bs<64>(f, cfg, maps, (int)G, stream_);
+    case 128: return launch_bs<128>(f, cfg, maps, (int)G, stream_);
     default: return MOE_LORA_ERR_UNSUPPORTED;
   }
 }

@@ -22,12 +22,15 @@ struct AlignArgs {
   int max_num_tokens_padded, max_num_m_blocks;
 };
 
+constexpr int kMaxSlices = 4;
+
 // Fused-stage inputs, as validated by the C-ABI layer.
 struct FusedArgs {
-  const uint16_t *x;       // bf16 [M, K]
-  const uint16_t *lora_a;  // bf16 [L, E, r, K]
-  const uint16_t *lora_b;  // bf16 [L, E, N, r]
-  uint16_t *y;             // bf16 [M, topk, N]
+  const uint16_t *x;                   // bf16 [M, K], or [M*topk, K] when x_per_pair
+  const uint16_t *lora_a[kMaxSlices];  // per slice: bf16 [L, E, r, K]
+  const uint16_t *lora_b[kMaxSlices];  // per slice: bf16 [L, E, N, r]
+  uint16_t *y;                         // bf16 [M, topk, ldy]; slice s at columns y_offset + s*N
+  const float *topk_weights;           // fp32 [M, topk] or null (no router-weight scaling)
   const int32_t *sorted_token_ids;
   const int32_t *expert_ids;
   const int32_t *num_tokens_post_padded;
@@ -37,7 +40,28 @@ struct FusedArgs {
   int M, topk, num_experts, K, N, rank, max_loras, num_active_loras, block_size;
   int max_num_tokens_padded, max_num_m_blocks;
   int add_inputs;
+  int num_slices;
+  int x_per_pair;
+  int ldy, y_offset;
 };
+
+// Device helpers for the per-slice operands and the pair's rows.
+__device__ __forceinline__ const uint16_t *slice_a(const FusedArgs &p, int s) {
+  return s == 0 ? p.lora_a[0] : (s == 1 ? p.lora_a[1] : (s == 2 ? p.lora_a[2] : p.lora_a[3]));
+}
+__device__ __forceinline__ const uint16_t *slice_b(const FusedArgs &p, int s) {
+  return s == 0 ? p.lora_b[0] : (s == 1 ? p.lora_b[1] : (s == 2 ? p.lora_b[2] : p.lora_b[3]));
+}
+// Row of x that pair f reads.
+__device__ __forceinline__ int x_row(const FusedArgs &p, int f) { return p.x_per_pair ? f : f / p.topk; }
+// First element of slice s's output columns in pair f's row of y.
+__device__ __forceinline__ size_t y_base(const FusedArgs &p, int f, int s) {
+  return (size_t)f * p.ldy + p.y_offset + (size_t)s * p.N;
+}
+// Router weight of pair f (1 when there are none).
+__device__ __forceinline__ float route_weight(const FusedArgs &p, int f) {
+  return p.topk_weights ? __ldg(p.topk_weights + f) : 1.f;
+}
 
 // Upper bound on the number of blocks all active slots can produce together:
 // every pair belongs to at most one slot, so the blocks are at most

@@ -49,14 +49,20 @@ int encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint
   return res == CUDA_SUCCESS ? 0 : MOE_LORA_ERR_LAUNCH;
 }
 
-int make_tensor_maps(const FusedArgs &f, const Cfg &cfg, CUtensorMap *ta, CUtensorMap *tb) {
+int make_tensor_maps(const FusedArgs &f, const Cfg &cfg, TmapSet *maps) {
   const uint64_t LE = (uint64_t)f.max_loras * f.num_experts;
-  if (int st = encode_3d(ta, f.lora_a, (uint64_t)f.K, (uint64_t)f.rank, LE, kTileK, (uint32_t)cfg.r_pad,
-                         CU_TENSOR_MAP_SWIZZLE_128B))
-    return st;
   const CUtensorMapSwizzle bsw = cfg.ka == 64 ? CU_TENSOR_MAP_SWIZZLE_128B
                                               : (cfg.ka == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B);
-  return encode_3d(tb, f.lora_b, (uint64_t)f.rank, (uint64_t)f.N, LE, (uint32_t)cfg.ka, kTileN, bsw);
+  for (int s = 0; s < kMaxSlices; ++s) {
+    const int src = s < f.num_slices ? s : 0;   // unused entries repeat slice 0
+    if (int st = encode_3d(&maps->a[s], f.lora_a[src], (uint64_t)f.K, (uint64_t)f.rank, LE, kTileK,
+                           (uint32_t)cfg.r_pad, CU_TENSOR_MAP_SWIZZLE_128B))
+      return st;
+    if (int st = encode_3d(&maps->b[s], f.lora_b[src], (uint64_t)f.rank, (uint64_t)f.N, LE, (uint32_t)cfg.ka, kTileN,
+                           bsw))
+      return st;
+  }
+  return 0;
 }
 
 int plan(const FusedArgs &f, const DeviceInfo &dev, int consumer_bytes, int t_bufs_max, Cfg *cfg) {

@@ -3,11 +3,14 @@
 // kernel (fused_tcgen05.cu) and the CUDA-core streaming kernel
 // (fused_stream_cc.cu).
 //
-// The work of a call is the list of (block, 128-column tile) pairs over all
-// blocks of all listed slots (vLLM PR #32005: the grid is sized by the active
-// LoRAs).  Each persistent CTA takes one contiguous, equal share of that list.
-// For every block it touches it needs that block's rank-r intermediate
-// (the shrink over all of K), then it produces its tiles of the block.
+// The work of a call is the list of (block, slice, 128-column tile) triples
+// over all blocks of all listed slots (vLLM PR #32005: the grid is sized by the
+// active LoRAs) and all adapter slices.  A (block, slice) pair is a "unit";
+// units are numbered block-major (unit = block * num_slices + slice) so that
+// the slices of one block, which gather the same x rows, run back to back.
+// Each persistent CTA takes one contiguous, equal share of that list.  For
+// every unit it touches it needs that unit's rank-r intermediate (the shrink
+// over all of K), then it produces its tiles of the unit.
 //
 // Two producers feed the consumers through shared-memory rings guarded by
 // mbarriers:
@@ -53,6 +56,12 @@ struct Cfg {
   int kt_total, nt_total;
 };
 
+// The A and B tensor maps of every slice (kernel parameter).
+struct TmapSet {
+  CUtensorMap a[kMaxSlices];
+  CUtensorMap b[kMaxSlices];
+};
+
 struct Meta {
   uint64_t full_sh[kMaxStages], empty_sh[kMaxStages];
   uint64_t full_ex[kMaxStages], empty_ex[kMaxStages];
@@ -65,6 +74,7 @@ struct Meta {
   int prefix[kMaxSlots + 1];
   int prod_f[128];    // expand producer's copy of the current block's pair ids (-1 = padding)
   int epi_f[128];     // consumers' copy
+  float epi_w[128];   // consumers: router weight of each row's pair
   int cpx[128];       // consumers: rows (positions in the block) of the real pairs, in order
   int wcount[16];
 };
@@ -95,13 +105,15 @@ __device__ __forceinline__ int find_slot(const int *prefix, int nact, int item) 
 }
 
 struct BlockRef {
-  int l, e;
-  const int32_t *ids;
+  int l, e, s;          // LoRA, expert and adapter slice of the unit
+  const int32_t *ids;   // the block's pair ids
 };
 
 template <int BS>
-__device__ __forceinline__ BlockRef block_ref(const FusedArgs &p, const Meta &meta, int gb) {
+__device__ __forceinline__ BlockRef block_ref(const FusedArgs &p, const Meta &meta, int unit) {
   BlockRef br;
+  const int gb = unit / p.num_slices;
+  br.s = unit - gb * p.num_slices;
   const int z = find_slot(meta.prefix, p.num_active_loras, gb);
   br.l = __ldg(p.lora_ids + z);
   const int b = gb - meta.prefix[z];
@@ -131,7 +143,8 @@ __device__ __forceinline__ void slot_prefix(const FusedArgs &p, Meta &meta) {
   }
 }
 
-// This CTA's share [t0, t1) of the (block, tile) list and the blocks it touches.
+// This CTA's share [t0, t1) of the (unit, tile) list and the units it touches
+// (gb0..gb1 number units).
 struct Range {
   long long t0, t1;
   int gb0, gb1;
@@ -140,9 +153,9 @@ struct Range {
   __device__ int tile_hi(int gb) const { return (int)min(t1 - (long long)gb * nt_total, (long long)nt_total); }
 };
 
-__device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int nt_total) {
+__device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int num_slices, int nt_total) {
   Range rg;
-  const long long total = (long long)meta.prefix[nact] * nt_total;
+  const long long total = (long long)meta.prefix[nact] * num_slices * nt_total;
   rg.t0 = total * blockIdx.x / gridDim.x;
   rg.t1 = total * (blockIdx.x + 1) / gridDim.x;
   rg.nt_total = nt_total;
@@ -157,7 +170,7 @@ __device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int nt_to
 // k-tiles later, once its copies are complete and fenced for async-proxy
 // readers.
 template <int BS>
-__device__ void shrink_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, const CUtensorMap *tmap_a,
+__device__ void shrink_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, const TmapSet *maps,
                                 uint8_t *sh_base, const Range &rg, int me) {
   const int lane = threadIdx.x & 31;
   const int K = p.K, E = p.num_experts, P = p.M * p.topk;
@@ -171,11 +184,12 @@ __device__ void shrink_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, 
     const bool e_ok = br.e >= 0 && br.e < E;
     if (!e_ok && lane == 0 && me == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
     const int le = br.l * E + (e_ok ? br.e : 0);
+    const CUtensorMap *tmap_a = &maps->a[br.s];
     int xrow[kRowsPerLane];
 #pragma unroll
     for (int i = 0; i < kRowsPerLane; ++i) {
       const int f = __ldg(br.ids + (lane >> 3) + 4 * i);
-      xrow[i] = (f >= 0 && f < P && e_ok) ? f / p.topk : -1;
+      xrow[i] = (f >= 0 && f < P && e_ok) ? x_row(p, f) : -1;
     }
     for (int kt = 0; kt < cfg.kt_total; ++kt, ++sh_iter) {
       if ((int)(sh_iter & 1) != me) continue;
@@ -222,7 +236,7 @@ __device__ void shrink_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, 
 // lane % 16 of rows lane/16 + 2i, real pairs only) by cp.async.  The row ids
 // are read before any copy is issued so that the copies go out back to back.
 template <int BS>
-__device__ void expand_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, const CUtensorMap *tmap_b,
+__device__ void expand_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, const TmapSet *maps,
                                 uint8_t *ex_base, const Range &rg) {
   const int lane = threadIdx.x & 31;
   const int E = p.num_experts, N = p.N, P = p.M * p.topk;
@@ -232,6 +246,8 @@ __device__ void expand_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, 
   for (int gb = rg.gb0; gb <= rg.gb1; ++gb) {
     const BlockRef br = block_ref<BS>(p, meta, gb);
     const int le = br.l * E + ((br.e >= 0 && br.e < E) ? br.e : 0);
+    const CUtensorMap *tmap_b = &maps->b[br.s];
+    const int s_col = p.y_offset + br.s * N;   // this slice's first output column
     __syncwarp();
     for (int pr = lane; pr < BS; pr += 32) {
       const int f = __ldg(br.ids + pr);
@@ -261,7 +277,8 @@ __device__ void expand_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, 
 #pragma unroll
           for (int i = 0; i < kRows; ++i)
             if (fr[i] >= 0)
-              cp_async_16(yt + ((lane >> 4) + 2 * i) * (kTileN * 2) + c16 * 16, p.y + (size_t)fr[i] * N + nn, 16u);
+              cp_async_16(yt + ((lane >> 4) + 2 * i) * (kTileN * 2) + c16 * 16,
+                          p.y + (size_t)fr[i] * p.ldy + s_col + nn, 16u);
         }
       }
       cp_async_mbar_arrive_noinc(&meta.full_ex[s]);
@@ -274,9 +291,9 @@ __device__ void expand_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, 
 int encode_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
               CUtensorMapSwizzle swizzle);
 
-// Tensor maps of A ([L*E, r, K], 64 x r_pad boxes, 128-byte swizzle) and B
-// ([L*E, N, r], ka x 128 boxes, swizzle matched to ka).
-int make_tensor_maps(const FusedArgs &f, const Cfg &cfg, CUtensorMap *ta, CUtensorMap *tb);
+// Tensor maps of every slice's A ([L*E, r, K], 64 x r_pad boxes, 128-byte
+// swizzle) and B ([L*E, N, r], ka x 128 boxes, swizzle matched to ka).
+int make_tensor_maps(const FusedArgs &f, const Cfg &cfg, TmapSet *maps);
 
 // Fill the geometry of cfg (r_pad, ka, stage sizes, tile counts) and choose
 // ring depths for a consumer region of `consumer_bytes` (per T buffer, up to

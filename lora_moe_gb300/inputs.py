@@ -15,7 +15,13 @@ trained weight is used: every value is drawn from numpy's PCG64 generator
     active LoRA set -> topk_ids -> token_lora_mapping -> x -> A -> B -> y_in
 
 Value distributions: x ~ N(0,1); A[l,e] ~ N(0, 1/K) (K = input dim of the
-adapter); B[l,e] ~ N(0, 1/r); y_in ~ N(0,1).  Normals are drawn as float32 and
+adapter); B[l,e] ~ N(0, 1/r); y_in ~ N(0,1).  The options of the general fused
+call (make_ex_inputs) draw from a second stream, seeded [seed, 1], in the order
+
+    x per pair -> A and B of slices 1.. -> router weights -> wide y_in
+
+with router weights a softmax over each token's top-k of N(0,1) draws (float32,
+positive, summing to 1 per token, like a router's top-k probabilities).  Normals are drawn as float32 and
 rounded to bf16 with round-to-nearest-even.  Adapter slots that are not in the
 active set are filled with a bf16 quiet NaN (0x7FC0) so that any read of an
 inactive slot shows up in the output.
@@ -182,3 +188,48 @@ def make_inputs(w: Workload, with_tensors: bool = True) -> Inputs:
     y = _normal_bf16(rng, w.M * w.topk * N, 1.0).reshape(w.M, w.topk, N)
     return Inputs(w, lora_ids, topk_ids, mapping, x, a, b, y)
 
+
+@dataclasses.dataclass
+class ExInputs:
+    """Inputs of the general fused call: slices, rows per pair, weights, offset."""
+
+    base: Inputs                        # routing; slice 0's adapters are base.lora_a / base.lora_b
+    x: np.ndarray                       # uint16 [M, K], or [M*topk, K] when x_per_pair
+    lora_a: list                        # per slice: uint16 [max_loras, E, r, K]
+    lora_b: list                        # per slice: uint16 [max_loras, E, N, r]
+    topk_weights: Optional[np.ndarray]  # float32 [M, topk] or None
+    y_in: np.ndarray                    # uint16 [M, topk, ldy]
+    x_per_pair: bool
+    y_offset: int
+
+
+def make_ex_inputs(w: Workload, num_slices: int = 1, x_per_pair: bool = False, routed_weights: bool = False,
+                   y_offset: int = 0, ldy: Optional[int] = None) -> ExInputs:
+    base = make_inputs(w)
+    rng = np.random.default_rng([w.seed, 1])
+    L, E, r, K, N = w.max_loras, w.E, w.rank, w.K, w.N
+    if ldy is None:
+        ldy = y_offset + num_slices * N
+    x = base.x
+    if x_per_pair:
+        x = _normal_bf16(rng, w.M * w.topk * K, 1.0).reshape(w.M * w.topk, K)
+    lora_a, lora_b = [base.lora_a], [base.lora_b]
+    for _ in range(1, num_slices):
+        a = np.full((L, E, r, K), BF16_QNAN, dtype=np.uint16)
+        for l in base.lora_ids:
+            a[l] = _normal_bf16(rng, E * r * K, 1.0 / np.sqrt(K)).reshape(E, r, K)
+        b = np.full((L, E, N, r), BF16_QNAN, dtype=np.uint16)
+        for l in base.lora_ids:
+            b[l] = _normal_bf16(rng, E * N * r, 1.0 / np.sqrt(r)).reshape(E, N, r)
+        lora_a.append(a)
+        lora_b.append(b)
+    weights = None
+    if routed_weights:
+        g = rng.standard_normal((w.M, w.topk), dtype=np.float32)
+        g = np.exp(g - g.max(axis=1, keepdims=True))
+        weights = (g / g.sum(axis=1, keepdims=True)).astype(np.float32)
+    if ldy == N and y_offset == 0:
+        y = base.y_in
+    else:
+        y = _normal_bf16(rng, w.M * w.topk * ldy, 1.0).reshape(w.M, w.topk, ldy)
+    return ExInputs(base, x, lora_a, lora_b, weights, y, x_per_pair, y_offset)

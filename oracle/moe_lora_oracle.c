@@ -53,6 +53,26 @@
  *  3. oracle_moe_lora_fused_sampled: the same definition evaluated only at a
  *     caller-chosen list of pairs and output columns, for checks at full size.
  *
+ *  4. oracle_moe_lora_fused_ex: the same definition with the options the
+ *     pages name around it: router-weight scaling (mul_routed_weight with
+ *     topk_weights, prhub.com.cn summary of vLLM PR #42290, step 2, and the
+ *     mul_routed_weight / offset arguments in the diff of vLLM PR #32005 to
+ *     fused_moe_lora_op.py), input rows per pair (the w2 stage's input is one
+ *     activation row per (token, expert) pair), several adapter slices per
+ *     layer (num_slices; the gate and up projections of w13 each have their
+ *     own A and B) and an output column offset.  Readings where the pages are
+ *     silent:
+ *       - the router weight multiplies the LoRA delta only, not y_in:
+ *             out = (add_inputs ? y_in : 0) + w[f] * sum_j B[n][j] * t[j];
+ *       - with x_per_pair, the input row of pair f is row f of x
+ *         ([M*topk][K]); otherwise row m = f / topk of x ([M][K]);
+ *       - slice s has its own A_s [L][E][r][K] and B_s [L][E][N][r] and its
+ *         own rank-r intermediate t_s; its N columns land at output columns
+ *         y_offset + s*N + n of a row of ldy columns;
+ *       - output columns that no slice writes keep y_in (either mode), and
+ *         uncovered pairs keep their whole row.
+ *     It can evaluate all pairs or a caller-chosen list of pairs.
+ *
  * Layouts (row-major, bf16 carried as raw uint16 bit patterns):
  *   topk_ids [M][topk] int32, token_lora_mapping [M] int32, lora_ids
  *   [num_active_loras] int32, x [M][K], lora_a [max_loras][E][r][K],
@@ -287,6 +307,47 @@ int oracle_moe_lora_fused_sampled(const uint16_t *x, const uint16_t *lora_a,
             const double delta = expand_one_column(
                 lora_b + ((int64_t)l * num_experts + e) * N * rank, n, rank, t);
             o[c] = (add_inputs ? bf16_value(yin[n]) : 0.0) + delta;
+        }
+    }
+    free(t);
+    return 0;
+}
+
+int oracle_moe_lora_fused_ex(const uint16_t *x, int x_per_pair,
+                             const uint16_t *const *lora_a, const uint16_t *const *lora_b,
+                             int num_slices, const uint16_t *y_in, int ldy, int y_offset,
+                             const float *topk_weights, const int32_t *topk_ids,
+                             const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                             const int32_t *adapter_enabled, int M, int topk, int num_experts,
+                             int K, int N, int rank, int max_loras, int num_active_loras,
+                             int add_inputs, const int32_t *pairs, int num_selected,
+                             double *out /* [num_selected, or M*topk if pairs is NULL][ldy] */)
+{
+    double *t = malloc(sizeof(double) * (size_t)(rank > 0 ? rank : 1));
+    if (!t)
+        return ORACLE_NOMEM;
+    const int rows = pairs ? num_selected : M * topk;
+    for (int i = 0; i < rows; ++i) {
+        const int f = pairs ? pairs[i] : i;
+        const int m = f / topk;
+        const uint16_t *yin = y_in + (int64_t)f * ldy;
+        double *o = out + (int64_t)i * ldy;
+        for (int c = 0; c < ldy; ++c)
+            o[c] = bf16_value(yin[c]);
+        int l, e;
+        if (!pair_is_covered(f, topk_ids, token_lora_mapping, lora_ids, adapter_enabled,
+                             topk, num_experts, max_loras, num_active_loras, &l, &e))
+            continue;
+        const uint16_t *x_row = x + (int64_t)(x_per_pair ? f : m) * K;
+        const double w = topk_weights ? (double)topk_weights[f] : 1.0;
+        for (int s = 0; s < num_slices; ++s) {
+            shrink_one_pair(x_row, lora_a[s] + ((int64_t)l * num_experts + e) * rank * K, K, rank, t);
+            const uint16_t *b_le = lora_b[s] + ((int64_t)l * num_experts + e) * N * rank;
+            for (int n = 0; n < N; ++n) {
+                const int c = y_offset + s * N + n;
+                const double delta = expand_one_column(b_le, n, rank, t);
+                o[c] = (add_inputs ? bf16_value(yin[c]) : 0.0) + w * delta;
+            }
         }
     }
     free(t);

@@ -41,6 +41,11 @@ def _load():
             lib.oracle_moe_lora_fused_sampled.argtypes = [
                 _u16p, _u16p, _u16p, _u16p, _i32p, _i32p, _i32p, opt_i32,
                 I, I, I, I, I, I, I, I, I, _i32p, I, _i32p, I, _f64p]
+            lib.oracle_moe_lora_fused_ex.restype = I
+            lib.oracle_moe_lora_fused_ex.argtypes = [
+                _u16p, I, ctypes.POINTER(ctypes.c_void_p), ctypes.POINTER(ctypes.c_void_p), I,
+                _u16p, I, I, ctypes.c_void_p, _i32p, _i32p, _i32p, opt_i32,
+                I, I, I, I, I, I, I, I, I, ctypes.c_void_p, I, _f64p]
             _lib = lib
     return _lib
 
@@ -138,6 +143,53 @@ def fused_sampled(x, lora_a, lora_b, y_in, topk_ids, token_lora_mapping, lora_id
         topk_ids.reshape(-1), _c32(token_lora_mapping), _c32(lora_ids), en,
         M, topk, E, K, N, r, L, len(lora_ids), int(bool(add_inputs)),
         pairs, len(pairs), columns, len(columns), out.reshape(-1))
+    del keep
+    assert st == 0
+    return out
+
+
+def fused_ex(x, lora_a, lora_b, y_in, topk_ids, token_lora_mapping, lora_ids,
+             add_inputs=True, adapter_enabled=None, topk_weights=None,
+             x_per_pair=False, y_offset=0, pairs=None):
+    """The fused definition with its options: router weights, input rows per
+    pair, several adapter slices and an output column offset.
+
+    lora_a / lora_b: one array per slice ([L, E, r, K] / [L, E, N, r]), or a
+    single array for one slice.  x: [M*topk, K] if x_per_pair else [M, K].
+    y_in: [M, topk, ldy].  topk_weights: float32 [M, topk] or None.
+    pairs: flat pair indices to evaluate (None: every pair).
+
+    Returns float64 [M, topk, ldy], or [len(pairs), ldy] when pairs is given."""
+    if not isinstance(lora_a, (list, tuple)):
+        lora_a, lora_b = [lora_a], [lora_b]
+    lora_a = [np.ascontiguousarray(a, np.uint16) for a in lora_a]
+    lora_b = [np.ascontiguousarray(b, np.uint16) for b in lora_b]
+    S = len(lora_a)
+    assert S >= 1 and len(lora_b) == S
+    x = np.ascontiguousarray(x, np.uint16)
+    y_in = np.ascontiguousarray(y_in, np.uint16)
+    topk_ids = _c32(topk_ids)
+    M, topk = topk_ids.shape
+    L, E, r, K = lora_a[0].shape
+    N = lora_b[0].shape[2]
+    for a, b in zip(lora_a, lora_b):
+        assert a.shape == (L, E, r, K) and b.shape == (L, E, N, r)
+    assert x.shape == ((M * topk if x_per_pair else M), K)
+    ldy = y_in.shape[-1]
+    assert y_in.shape == (M, topk, ldy) and 0 <= y_offset and y_offset + S * N <= ldy
+    a_ptrs = (ctypes.c_void_p * S)(*[a.ctypes.data for a in lora_a])
+    b_ptrs = (ctypes.c_void_p * S)(*[b.ctypes.data for b in lora_b])
+    w = None if topk_weights is None else np.ascontiguousarray(topk_weights, np.float32)
+    if w is not None:
+        assert w.shape == (M, topk)
+    sel = None if pairs is None else _c32(pairs)
+    out = np.empty(((M, topk, ldy) if sel is None else (len(sel), ldy)), np.float64)
+    keep, en = _opt(adapter_enabled)
+    st = _load().oracle_moe_lora_fused_ex(
+        x.reshape(-1), int(bool(x_per_pair)), a_ptrs, b_ptrs, S, y_in.reshape(-1), ldy, y_offset,
+        None if w is None else w.ctypes.data, topk_ids.reshape(-1), _c32(token_lora_mapping),
+        _c32(lora_ids), en, M, topk, E, K, N, r, L, len(lora_ids), int(bool(add_inputs)),
+        None if sel is None else sel.ctypes.data, 0 if sel is None else len(sel), out.reshape(-1))
     del keep
     assert st == 0
     return out

@@ -103,3 +103,57 @@ def test_fused_argument_errors():
     p = ctypes.addressof(buf)
     p1 = ((p + 15) & ~15) + 2                     # misaligned on purpose (host memory, never dereferenced)
     assert _fused(x=p1, a=p1, b=p1, y=p1, sorted=p1, experts=p1, ntpp=p1, lora_ids=p1) == 3
+
+
+def _fused_ex(slices=1, a_ptrs=None, b_ptrs=None, **kw):
+    P = ctypes.c_void_p
+    if a_ptrs is None:
+        a_ptrs = (P * max(slices, 1))()
+    if b_ptrs is None:
+        b_ptrs = (P * max(slices, 1))()
+    args = dict(x=None, x_per_pair=0, a=a_ptrs, b=b_ptrs, S=slices, y=None, ldy=512, y_off=0, w=None,
+                sorted=None, experts=None, ntpp=None, lora_ids=None, enabled=None, M=16, topk=2, E=8, K=256,
+                N=512, r=8, L=2, nact=2, bs=16, cap=152, capb=10, add=1, path=0, err=None, stream=None)
+    args.update(kw)
+    return B.lib().moe_lora_fused_shrink_expand_ex(*args.values())
+
+
+def test_fused_ex_argument_errors():
+    assert _fused_ex(slices=0) == 1                   # no slice
+    assert _fused_ex(slices=5, ldy=5 * 512) == 1      # more than MOE_LORA_MAX_SLICES
+    assert _fused_ex(slices=2, ldy=512) == 1          # slices do not fit the row
+    assert _fused_ex(y_off=8, ldy=512) == 1           # offset pushes the slice past the row
+    assert _fused_ex(y_off=-8, ldy=1024) == 1
+    assert _fused_ex(ldy=1028, y_off=0) == 3          # row stride not a 16-byte multiple
+    assert _fused_ex(ldy=1024, y_off=4) == 3          # offset not a 16-byte multiple
+    assert _fused_ex(a=None) == 1                     # no slice pointer arrays
+    assert _fused_ex(r=12, path=4) == 2               # streaming kernel needs rank % 8 == 0
+    assert _fused_ex(slices=2, ldy=1024, nact=0) == 0 # zero grid
+    assert _fused_ex(slices=3, ldy=3 * 512, M=0) == 0 # empty batch
+    assert _fused_ex(slices=2, ldy=1024) == 1         # NULL buffers
+    buf = ctypes.create_string_buffer(64)
+    p = ctypes.addressof(buf)
+    p0 = (p + 15) & ~15
+    P = ctypes.c_void_p
+    ok = dict(x=p0, y=p0, sorted=p0, experts=p0, ntpp=p0, lora_ids=p0)
+    # misaligned slice pointer or weights (host memory, never dereferenced)
+    assert _fused_ex(slices=2, ldy=1024, a_ptrs=(P * 2)(p0, p0 + 2), b_ptrs=(P * 2)(p0, p0), **ok) == 3
+    assert _fused_ex(slices=1, w=p0 + 2, a_ptrs=(P * 1)(p0), b_ptrs=(P * 1)(p0), **ok) == 3
+    assert _fused_ex(slices=2, ldy=1024, a_ptrs=(P * 2)(p0, None), b_ptrs=(P * 2)(p0, p0), **ok) == 1
+
+
+def test_fused_resolve_path():
+    R = B.lib().moe_lora_fused_resolve_path
+    # decode-sized, small adapters -> cluster kernel; many pairs -> tensor cores
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 0) == 3
+    assert R(8192, 2, 8, 4096, 28672, 16, 4, 64, 1, 0) == 2
+    # few pairs but large adapters (block bound x (K + N) x r x 2 bytes > 48 MB) -> tensor cores
+    assert R(64, 4, 128, 2880, 2880, 64, 6, 16, 1, 0) == 2
+    # rank % 8 != 0 keeps the CUDA cores
+    assert R(8192, 2, 8, 4096, 28672, 12, 4, 64, 1, 0) == 3
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 1) == 3   # CUDA_CORE -> cluster
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 4) == 4
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 2) == 2
+    assert R(16, 8, 128, 2048, 1536, 12, 2, 16, 1, 2) == -2  # tensor cores need rank % 8 == 0
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 5, 0) == -1  # too many slices
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 9) == -1

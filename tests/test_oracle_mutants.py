@@ -16,6 +16,7 @@ import oracle
 from oracle import oracle as oracle_impl
 
 import test_oracle_pins as pins
+import test_oracle_pins_ex as pins_ex
 
 SRC = os.path.join(os.path.dirname(oracle_impl.__file__), "moe_lora_oracle.c")
 
@@ -45,6 +46,18 @@ MUTANTS = [
     ("adapter_enabled ignored", "    if (adapter_enabled && !adapter_enabled[l])\n        return 0;\n", ""),
     ("wrong expert stride", "lora_a + ((int64_t)l * num_experts + e) * rank * K;",
      "lora_a + ((int64_t)e * num_experts + l) * rank * K;"),
+    # the general definition (router weights, rows per pair, slices, offset)
+    ("router weight also scales y_in", "o[c] = (add_inputs ? bf16_value(yin[c]) : 0.0) + w * delta;",
+     "o[c] = w * ((add_inputs ? bf16_value(yin[c]) : 0.0) + delta);"),
+    ("router weight indexed by token", "(double)topk_weights[f]", "(double)topk_weights[m * topk]"),
+    ("router weight ignored", "(double)topk_weights[f]", "1.0"),
+    ("rows per pair ignored", "(x_per_pair ? f : m)", "(m)"),
+    ("slice column stride dropped", "const int c = y_offset + s * N + n;", "const int c = y_offset + n;"),
+    ("column offset ignored", "const int c = y_offset + s * N + n;", "const int c = s * N + n;"),
+    ("first slice's A reused", "lora_a[s] + ", "lora_a[0] + "),
+    ("first slice's B reused", "lora_b[s] + ", "lora_b[0] + "),
+    ("unwritten columns cleared when overwriting", "            o[c] = bf16_value(yin[c]);",
+     "            o[c] = add_inputs ? bf16_value(yin[c]) : 0.0;"),
 ]
 
 PIN_TESTS = [
@@ -60,6 +73,11 @@ PIN_TESTS = [
     pins.test_fused_one_hot_adapters_copy_x,
     pins.test_fused_dense_special_case,
     pins.test_fused_uncovered_pairs_untouched_and_poison_unread,
+    pins_ex.test_fused_ex_worked_example,
+    pins_ex.test_fused_ex_per_pair_rows_as_tokens,
+    pins_ex.test_fused_ex_slices_are_independent_column_blocks,
+    pins_ex.test_fused_ex_router_weight_scales_the_delta_only,
+    pins_ex.test_fused_ex_integer_case_exact,
 ]
 
 
@@ -76,7 +94,8 @@ def _build_mutant(src_text, tmpdir):
 def _caught(so_path):
     lib = ctypes.CDLL(so_path)
     real = oracle_impl._load()
-    for name in ("oracle_moe_lora_align", "oracle_moe_lora_fused", "oracle_moe_lora_fused_sampled"):
+    for name in ("oracle_moe_lora_align", "oracle_moe_lora_fused", "oracle_moe_lora_fused_sampled",
+                 "oracle_moe_lora_fused_ex"):
         fn = getattr(lib, name)
         ref = getattr(real, name)
         fn.argtypes, fn.restype = ref.argtypes, ref.restype
