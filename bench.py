@@ -64,11 +64,13 @@ def parse():
     ap.add_argument("--slices", type=int, default=1, help="adapter slices per layer (general call)")
     ap.add_argument("--per-pair-x", action="store_true", help="one input row per pair (general call)")
     ap.add_argument("--routed-weight", action="store_true", help="scale by the router weight (general call)")
+    ap.add_argument("--naive", action="store_true",
+                    help="naive block assignment: the step is the fused call alone, one work item per pair")
     return ap.parse_args()
 
 
 def uses_ex(args):
-    return args.slices != 1 or args.per_pair_x or args.routed_weight
+    return args.slices != 1 or args.per_pair_x or args.routed_weight or args.naive
 
 
 def make_step_inputs(w, args):
@@ -82,7 +84,7 @@ def make_step_inputs(w, args):
 
 # --------------------------------------------------------------------------- roofline bookkeeping
 
-def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weight=False):
+def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weight=False, naive=False):
     """What the method must move / compute for one step, from the actual inputs.
 
     bytes = x rows of covered tokens (or covered pairs, with one input row per
@@ -104,8 +106,11 @@ def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weigh
     blocks = padded // w.block_size
     r = w.rank
     x_rows = P if per_pair_x else int(m_cov.sum())
+    # routing metadata the fused stage reads: the align outputs, or (naive
+    # block assignment) topk_ids and token_lora_mapping
+    meta = 4 * (w.M * w.topk + w.M) if naive else 4 * (padded + blocks + w.num_active_loras)
     fused_bytes = (2 * w.K * x_rows + slices * S * 2 * r * (w.K + w.N) + slices * P * w.N * 2 * 2
-                   + (4 * P if routed_weight else 0) + 4 * (padded + blocks + w.num_active_loras))
+                   + (4 * P if routed_weight else 0) + meta)
     align_bytes = 4 * w.M * w.topk + 4 * w.M + 4 * (padded + blocks + w.num_active_loras)
     return dict(pairs=P, segments=S, padded_rows=padded, blocks=blocks, fused_bytes=fused_bytes,
                 align_bytes=align_bytes, flops=2 * r * (w.K + w.N) * P * slices)
@@ -212,7 +217,8 @@ def max_over_ranks(pg, value, use_cuda):
 
 # --------------------------------------------------------------------------- CPU oracle timing
 
-def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: int = None, ex=None):
+def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: int = None, ex=None,
+                with_align=True):
     """Time the oracle's align (whole batch) and fused stage (a rotating subset
     of covered pairs, every column; the general definition when `ex` holds the
     general call's inputs) and scale to microseconds per full step.
@@ -231,7 +237,8 @@ def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: in
     t_start = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        oracle.align(inp.topk_ids, inp.token_lora_mapping, inp.lora_ids, w.E, w.max_loras, w.block_size)
+        if with_align:
+            oracle.align(inp.topk_ids, inp.token_lora_mapping, inp.lora_ids, w.E, w.max_loras, w.block_size)
         t1 = time.perf_counter()
         sel = cov_idx[(made * n + np.arange(n)) % max(1, len(cov_idx))] if len(cov_idx) else cov_idx
         if len(sel) and ex is not None:
@@ -253,8 +260,8 @@ def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: in
             break
     per_pair = t_fused / max(1, done_pairs)
     us = (t_align / made + per_pair * len(cov_idx)) * 1e6
-    desc = ("oracle align over the whole batch + oracle fused over %d of %d covered pairs per call "
-            "(all %d columns), %d calls, scaled to one full step" % (n, len(cov_idx), w.N, made))
+    desc = ("%soracle fused over %d of %d covered pairs per call (all %d columns), %d calls, scaled to one "
+            "full step" % ("oracle align over the whole batch + " if with_align else "", n, len(cov_idx), w.N, made))
     return us, desc, made
 
 
@@ -268,7 +275,7 @@ def run_ours(args, world, rank, local, pg):
     dev = torch.device("cuda", local)
     w = gen.WORKLOADS[args.workload]
     inp, ex = make_step_inputs(w, args)
-    counts = algorithmic_counts(inp, args.slices, args.per_pair_x, args.routed_weight)
+    counts = algorithmic_counts(inp, args.slices, args.per_pair_x, args.routed_weight, args.naive)
 
     def i32(a):
         return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
@@ -309,7 +316,13 @@ def run_ours(args, world, rank, local, pg):
 
     def fused(s):
         b = s["buf"]
-        if ex is None:
+        if args.naive:
+            B.moe_lora_fused_shrink_expand_naive(
+                s["x"], [s["a%d" % i] for i in range(args.slices)], [s["b%d" % i] for i in range(args.slices)],
+                s["y"], s["topk_ids"], s["mapping"], s["lora_ids"], w.max_loras, add_inputs=True,
+                topk_weights=s.get("w"), x_per_pair=ex.x_per_pair, y_offset=ex.y_offset, err_flag=err,
+                stream=stream)
+        elif ex is None:
             B.moe_lora_fused_shrink_expand(s["x"], s["a0"], s["b0"], s["y"], b.sorted_token_ids, b.expert_ids,
                                            b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
                                            add_inputs=True, path=args.path, err_flag=err, stream=stream)
@@ -322,7 +335,8 @@ def run_ours(args, world, rank, local, pg):
 
     def step(i):
         s = sets[i % NB]
-        align(s)
+        if not args.naive:
+            align(s)
         fused(s)
 
     if args.profile_steps:
@@ -397,7 +411,9 @@ def run_ours(args, world, rank, local, pg):
         return a.elapsed_time(b) * 1e3 / (reps * NB)   # us per call
 
     fused_us = kernel_time(fused, 1)
-    align_us = kernel_time(align, align_launches)
+    align_us = None if args.naive else kernel_time(align, align_launches)
+    if args.naive:
+        align_launches = 0
 
     # ---------------- end to end through the public API with host buffers
     e2e = None
@@ -424,7 +440,8 @@ def run_ours(args, world, rank, local, pg):
                 s["y"].view(torch.int16).copy_(host["y"], non_blocking=True)
                 if "w" in host:
                     s["w"].copy_(host["w"], non_blocking=True)
-            align(s)
+            if not args.naive:
+                align(s)
             fused(s)
             with torch.cuda.stream(stream):
                 out_host.copy_(s["y"].view(torch.int16), non_blocking=True)
@@ -451,6 +468,8 @@ def run_ours(args, world, rank, local, pg):
                                   args.slices, args.path)
     kernel_name = {B.PATH_TCGEN05: "fused_tcgen05_kernel", B.PATH_CUDA_CORE_CLUSTER: "fused_cuda_core_kernel",
                    B.PATH_CUDA_CORE_STREAM: "fused_stream_cc_kernel"}[kernel]
+    if args.naive:
+        kernel_name = "fused_cuda_core_kernel (naive block assignment)"
     return dict(ms=ms, clocks=clocks, fused_us=fused_us, align_us=align_us, counts=counts, NB=NB, l2=l2,
                 footprint=NB * per_set, kernel_name=kernel_name,
                 align_launches=align_launches, e2e=e2e, achieved=achieved, peak=peak, peak_kind=peak_kind,
@@ -461,7 +480,10 @@ def ex_config(args):
     """Config keys of the general call's options (none for the plain call)."""
     if not uses_ex(args):
         return {}
-    return {"num_slices": args.slices, "x_per_pair": bool(args.per_pair_x), "routed_weight": bool(args.routed_weight)}
+    d = {"num_slices": args.slices, "x_per_pair": bool(args.per_pair_x), "routed_weight": bool(args.routed_weight)}
+    if args.naive:
+        d["block_assignment"] = "naive (no align)"
+    return d
 
 
 def main():
@@ -477,12 +499,13 @@ def main():
             return
         inp, ex = make_step_inputs(w, args)
         # size the per-step sample so that W + K steps take a couple of minutes at most
-        probe_us, _, _ = time_oracle(inp, 0.5, 4, ex=ex)
+        wa = not args.naive
+        probe_us, _, _ = time_oracle(inp, 0.5, 4, ex=ex, with_align=wa)
         per_pair_budget = 120.0 / (args.steps + args.warmup)
         pairs_per_call = max(1, int(per_pair_budget / max(1e-9, probe_us * 1e-6 / max(1, algorithmic_counts(inp)["pairs"]))))
-        time_oracle(inp, 0, pairs_per_call, calls=args.warmup, ex=ex)
+        time_oracle(inp, 0, pairs_per_call, calls=args.warmup, ex=ex, with_align=wa)
         t0 = time.perf_counter()
-        us, desc, made = time_oracle(inp, 0, pairs_per_call, calls=args.steps, ex=ex)
+        us, desc, made = time_oracle(inp, 0, pairs_per_call, calls=args.steps, ex=ex, with_align=wa)
         wall = time.perf_counter() - t0
         line = {"impl": "reference", "metric": METRIC, "value": us, "unit": "us/call", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
@@ -506,7 +529,7 @@ def main():
     us_per_step = res["ms"] * 1e3 / (args.steps * world)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        us, desc, made = time_oracle(res["inp"], 12.0, 8, ex=res["ex"])
+        us, desc, made = time_oracle(res["inp"], 12.0, 8, ex=res["ex"], with_align=not args.naive)
         cpu = {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": desc}
     if rank != 0:
         if pg is not None:
@@ -528,7 +551,8 @@ def main():
                     "align_launches_per_call": res["align_launches"],
                     "fused_gbs": res["achieved"],
                     "fused_tflops": counts["flops"] / (res["fused_us"] * 1e-6) / 1e12,
-                    "align_gbs": counts["align_bytes"] / (res["align_us"] * 1e-6) / 1e9},
+                    "align_gbs": (counts["align_bytes"] / (res["align_us"] * 1e-6) / 1e9
+                                  if res["align_us"] else None)},
         "algorithmic": counts,
         "roofline": {"bound": "hbm", "kernel": res["kernel_name"], "achieved": res["achieved"], "peak": res["peak"],
                      "unit": "GB/s",

@@ -152,6 +152,26 @@ int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping,
                    int variant, int32_t *err_flag, void *stream);
 
 /*
+ * moe_align_block_size -- the plain (non-LoRA) MoE align: group all (token,
+ * top-k) pairs by expert into block_size-padded segments.  It is the
+ * single-slot case of moe_lora_align (one routine serves the LoRA and the
+ * non-LoRA callers: vLLM PR #29257, section Purpose): every token belongs to
+ * the one slot, whose row is row 0.  Same output rules as moe_lora_align with
+ * max_loras = num_active_loras = 1:
+ *   sorted_token_ids [device] int32 [max_num_tokens_padded]
+ *   expert_ids       [device] int32 [max_num_m_blocks]
+ *   num_tokens_post_padded [device] int32 [1]
+ * workspace: moe_lora_align_workspace_bytes(M, topk, num_experts, 1,
+ * block_size, variant) bytes, [device], 16-byte aligned (may be NULL when
+ * that is 0).  Limits and errors as for moe_lora_align.
+ */
+int moe_align_block_size(const int32_t *topk_ids, int M, int topk, int num_experts, int block_size,
+                         int32_t *sorted_token_ids, int32_t *expert_ids, int32_t *num_tokens_post_padded,
+                         int max_num_tokens_padded, int max_num_m_blocks,
+                         void *workspace, size_t workspace_bytes, int variant,
+                         int32_t *err_flag, void *stream);
+
+/*
  * moe_lora_fused_shrink_expand -- apply each covered pair's adapter.
  *
  * Reads the align outputs of the same slots and, for every block b of every
@@ -237,6 +257,39 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair,
                                     int max_loras, int num_active_loras, int block_size,
                                     int max_num_tokens_padded, int max_num_m_blocks,
                                     int add_inputs, int path, int32_t *err_flag, void *stream);
+
+/*
+ * moe_lora_fused_shrink_expand_naive -- the general fused call without the
+ * align stage (naive block assignment: the one-shot kernel's grid of
+ * (num_tokens * top_k, num_slices, num_active_loras) programs, one per pair,
+ * in the prhub.com.cn summary of vLLM PR #42290, "Key source snippets"; the
+ * early-exit and zero-grid cases of its tests, "Implementation breakdown"
+ * step 4).  Each (token, top-k) pair f is its own work item: l =
+ * token_lora_mapping[f / topk], e = topk_ids[f]; the pair is covered when l is
+ * one of lora_ids[0, num_active_loras), its adapter is enabled and
+ * 0 <= e < num_experts, and then gets exactly the update of
+ * moe_lora_fused_shrink_expand_ex.  Uncovered pairs exit at once and are not
+ * touched.  A covered token with an expert id outside [0, num_experts) is
+ * reported as MOE_LORA_DEVERR_EXPERT_ID, a lora_ids entry outside
+ * [0, max_loras) as MOE_LORA_DEVERR_LORA_ID.  Pairs that share an adapter
+ * each read it (from L2 after the first), so this path suits batches with
+ * few pairs per (LoRA, expert), i.e. decode.  Runs on CUDA cores (the
+ * cluster kernel).
+ *
+ *   topk_ids          [device] int32 [M, topk]
+ *   token_lora_mapping [device] int32 [M] (-1: no adapter)
+ *   the rest as for moe_lora_fused_shrink_expand_ex.
+ */
+int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair,
+                                       const moe_lora_bf16 *const *lora_a,
+                                       const moe_lora_bf16 *const *lora_b, int num_slices,
+                                       moe_lora_bf16 *y, int ldy, int y_offset,
+                                       const float *topk_weights, const int32_t *topk_ids,
+                                       const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                                       const int32_t *adapter_enabled, int M, int topk,
+                                       int num_experts, int K, int N, int rank, int max_loras,
+                                       int num_active_loras, int add_inputs, int32_t *err_flag,
+                                       void *stream);
 
 /*
  * moe_lora_fused_resolve_path -- the kernel a fused call with these sizes

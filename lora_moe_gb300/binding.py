@@ -66,6 +66,11 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_fused_shrink_expand_ex.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P), I, P, I, I, P,
                                                           P, P, P, P, P,
                                                           I, I, I, I, I, I, I, I, I, I, I, I, I, P, P]
+            L.moe_align_block_size.restype = I
+            L.moe_align_block_size.argtypes = [P, I, I, I, I, P, P, P, I, I, P, S, I, P, P]
+            L.moe_lora_fused_shrink_expand_naive.restype = I
+            L.moe_lora_fused_shrink_expand_naive.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P), I, P, I, I,
+                                                             P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
             L.moe_lora_fused_resolve_path.restype = I
             L.moe_lora_fused_resolve_path.argtypes = [I] * 10
             _lib = L
@@ -133,6 +138,21 @@ def moe_lora_align(topk_ids, token_lora_mapping, lora_ids, num_experts, max_lora
 
 
 STATIC_WORKSPACE_BYTES = 4 << 20
+
+
+def moe_align_block_size(topk_ids, num_experts, block_size, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                         workspace=None, variant=ALIGN_AUTO, err_flag=None, stream=None):
+    """The plain (non-LoRA) MoE align on device tensors: outputs are
+    sorted_token_ids [cap], expert_ids [capb], num_tokens_post_padded [1]."""
+    M, topk = topk_ids.shape
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    st = lib().moe_align_block_size(
+        _ptr(topk_ids, torch.int32, "topk_ids"), M, topk, num_experts, block_size,
+        _ptr(sorted_token_ids, torch.int32, "sorted_token_ids"), _ptr(expert_ids, torch.int32, "expert_ids"),
+        _ptr(num_tokens_post_padded, torch.int32, "num_tokens_post_padded"),
+        sorted_token_ids.numel(), expert_ids.numel(), _ptr(workspace, name="workspace"), nbytes, variant,
+        _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+    _check(st, "moe_align_block_size")
 
 
 def moe_lora_align_static_workspace(topk_ids, token_lora_mapping, lora_ids, num_experts, max_loras, block_size,
@@ -225,6 +245,43 @@ def moe_lora_fused_shrink_expand_ex(x, lora_a, lora_b, y, sorted_token_ids, expe
         sorted_token_ids.shape[-1], expert_ids.shape[-1], int(bool(add_inputs)), path,
         _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
     _check(st, "moe_lora_fused_shrink_expand_ex")
+
+
+def moe_lora_fused_shrink_expand_naive(x, lora_a, lora_b, y, topk_ids, token_lora_mapping, lora_ids, max_loras,
+                                       add_inputs=True, adapter_enabled=None, topk_weights=None, x_per_pair=False,
+                                       y_offset=0, err_flag=None, stream=None):
+    """moe_lora_fused_shrink_expand_naive (no align: one work item per pair) on
+    device tensors; y [M, topk, ldy] is updated in place.  lora_a / lora_b: a
+    tensor or a list of per-slice tensors."""
+    if isinstance(lora_a, torch.Tensor):
+        lora_a, lora_b = [lora_a], [lora_b]
+    S = len(lora_a)
+    if S < 1 or len(lora_b) != S:
+        raise ValueError("lora_a and lora_b need the same number of slices")
+    L, E, r, K = lora_a[0].shape
+    N = lora_b[0].shape[2]
+    for a, b in zip(lora_a, lora_b):
+        if tuple(a.shape) != (L, E, r, K) or tuple(b.shape) != (L, E, N, r):
+            raise ValueError("inconsistent slice shapes")
+    M, topk = topk_ids.shape
+    if y.dim() != 3 or y.shape[0] != M or y.shape[1] != topk:
+        raise ValueError("y must be [M, topk, ldy]")
+    if tuple(x.shape) != ((M * topk if x_per_pair else M), K) or token_lora_mapping.numel() != M:
+        raise ValueError("inconsistent shapes")
+    if topk_weights is not None and topk_weights.numel() != M * topk:
+        raise ValueError("topk_weights must be [M, topk]")
+    if max_loras != L:
+        raise ValueError("max_loras must equal the adapters' first dimension")
+    bf = torch.bfloat16
+    a_ptrs = (ctypes.c_void_p * S)(*[_ptr(a, bf, "lora_a") for a in lora_a])
+    b_ptrs = (ctypes.c_void_p * S)(*[_ptr(b, bf, "lora_b") for b in lora_b])
+    st = lib().moe_lora_fused_shrink_expand_naive(
+        _ptr(x, bf, "x"), int(bool(x_per_pair)), a_ptrs, b_ptrs, S, _ptr(y, bf, "y"), y.shape[2], y_offset,
+        _ptr(topk_weights, torch.float32, "topk_weights"), _ptr(topk_ids, torch.int32, "topk_ids"),
+        _ptr(token_lora_mapping, torch.int32, "token_lora_mapping"), _ptr(lora_ids, torch.int32, "lora_ids"),
+        _ptr(adapter_enabled, torch.int32, "adapter_enabled"), M, topk, E, K, N, r, L, lora_ids.numel(),
+        int(bool(add_inputs)), _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+    _check(st, "moe_lora_fused_shrink_expand_naive")
 
 
 class AlignBuffers:

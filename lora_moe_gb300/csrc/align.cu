@@ -40,10 +40,11 @@ constexpr int kScanThreads = 1024;              // one thread per expert (E <= 1
 constexpr int kMaxGlobalWarpRanges = 128;       // global variant: target warp ranges per slot
 
 // Expert of pair f for slot l, or -1 when the pair is not this slot's or its
-// expert is out of range (flagged once, in the counting pass).
+// expert is out of range (flagged once, in the counting pass).  Without a
+// token_lora_mapping every token belongs to the one slot (plain MoE align).
 __device__ __forceinline__ int pair_expert(const AlignArgs &a, int f, int l, bool flag) {
   const int m = f / a.topk;
-  if (__ldg(a.token_lora_mapping + m) != l) return -1;
+  if (a.token_lora_mapping && __ldg(a.token_lora_mapping + m) != l) return -1;
   const int e = __ldg(a.topk_ids + f);
   if (e < 0 || e >= a.num_experts) {
     if (flag) flag_error(a.err, MOE_LORA_DEVERR_EXPERT_ID);
@@ -54,8 +55,9 @@ __device__ __forceinline__ int pair_expert(const AlignArgs &a, int f, int l, boo
 
 // Slot z's LoRA index, or -1 when the slot is skipped (bad id: flagged;
 // disabled adapter: its num_tokens_post_padded is set to 0 by `writer`).
+// Without lora_ids, slot z is row z (plain MoE align: one slot, row 0).
 __device__ __forceinline__ int slot_lora(const AlignArgs &a, int z, bool writer) {
-  const int l = __ldg(a.lora_ids + z);
+  const int l = a.lora_ids ? __ldg(a.lora_ids + z) : z;
   if (l < 0 || l >= a.max_loras) {
     if (writer) flag_error(a.err, MOE_LORA_DEVERR_LORA_ID);
     return -1;

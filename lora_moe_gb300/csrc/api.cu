@@ -79,6 +79,101 @@ int resolve_align_variant(int M, int topk, int E, int variant) {
 
 }  // namespace
 
+// Both align entry points: a null token_lora_mapping puts every token in the
+// one slot, null lora_ids make slot z row z (the plain MoE align).
+static int align_impl(const int32_t *topk_ids, const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                   const int32_t *adapter_enabled, int M, int topk, int num_experts, int max_loras,
+                   int num_active_loras, int block_size, int32_t *sorted_token_ids, int32_t *expert_ids,
+                   int32_t *num_tokens_post_padded, int max_num_tokens_padded, int max_num_m_blocks,
+                   void *workspace, size_t workspace_bytes, int variant, int32_t *err_flag, void *stream) {
+  if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
+                            max_num_m_blocks))
+    return st;
+  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_GLOBAL) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_active_loras == 0) return MOE_LORA_OK;
+  if (!sorted_token_ids || !expert_ids || !num_tokens_post_padded) return MOE_LORA_ERR_INVALID_ARG;
+  if (M > 0 && !topk_ids) return MOE_LORA_ERR_INVALID_ARG;
+  const int v = resolve_align_variant(M, topk, num_experts, variant);
+  if (v == MOE_LORA_ALIGN_SMEM && !align_smem_fits(num_experts)) return MOE_LORA_ERR_UNSUPPORTED;
+  DeviceInfo dev;
+  if (int st = current_device_info(&dev)) return st;
+  AlignArgs a;
+  a.topk_ids = topk_ids;
+  a.token_lora_mapping = token_lora_mapping;
+  a.lora_ids = lora_ids;
+  a.adapter_enabled = adapter_enabled;
+  a.sorted_token_ids = sorted_token_ids;
+  a.expert_ids = expert_ids;
+  a.num_tokens_post_padded = num_tokens_post_padded;
+  a.err = err_flag;
+  a.M = M;
+  a.topk = topk;
+  a.num_experts = num_experts;
+  a.max_loras = max_loras;
+  a.num_active_loras = num_active_loras;
+  a.block_size = block_size;
+  a.max_num_tokens_padded = max_num_tokens_padded;
+  a.max_num_m_blocks = max_num_m_blocks;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (v == MOE_LORA_ALIGN_SMEM) return launch_align_smem(a, s);
+  const size_t need = align_global_workspace_bytes(M, topk, num_experts, num_active_loras);
+  if (!workspace || workspace_bytes < need) return MOE_LORA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MOE_LORA_ERR_MISALIGNED;
+  return launch_align_global(a, workspace, s);
+}
+
+// Checks and fills what both fused entry points (sorted and naive block
+// assignment) share: the operands, the options and the rank / size limits.
+// *empty is set when there is nothing to do (no active slot or no token).
+static int prepare_fused(const moe_lora_bf16 *x, int x_per_pair, const moe_lora_bf16 *const *lora_a,
+                         const moe_lora_bf16 *const *lora_b, int num_slices, moe_lora_bf16 *y, int ldy, int y_offset,
+                         const float *topk_weights, const int32_t *lora_ids, const int32_t *adapter_enabled, int M,
+                         int topk, int num_experts, int K, int N, int rank, int max_loras, int num_active_loras,
+                         int add_inputs, int32_t *err_flag, FusedArgs *out, bool *empty) {
+  if (K < 8 || N < 8 || rank < 1) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_slices < 1 || num_slices > kMaxSlices || !lora_a || !lora_b) return MOE_LORA_ERR_INVALID_ARG;
+  if (y_offset < 0 || ldy < 8 || (long long)y_offset + (long long)num_slices * N > ldy) return MOE_LORA_ERR_INVALID_ARG;
+  if (rank > kMaxRank || rank % 4 != 0) return MOE_LORA_ERR_UNSUPPORTED;
+  if (K % 8 != 0 || N % 8 != 0 || ldy % 8 != 0 || y_offset % 8 != 0) return MOE_LORA_ERR_MISALIGNED;
+  const long long x_rows = x_per_pair ? (long long)M * topk : (long long)M;
+  if (x_rows * K > INT32_MAX * 8LL || (long long)M * topk * ldy > INT32_MAX * 8LL) return MOE_LORA_ERR_UNSUPPORTED;
+  *empty = num_active_loras == 0 || M == 0;
+  if (*empty) return MOE_LORA_OK;
+  if (!x || !y || !lora_ids) return MOE_LORA_ERR_INVALID_ARG;
+  for (int s = 0; s < num_slices; ++s) {
+    if (!lora_a[s] || !lora_b[s]) return MOE_LORA_ERR_INVALID_ARG;
+    if (!aligned16(lora_a[s]) || !aligned16(lora_b[s])) return MOE_LORA_ERR_MISALIGNED;
+  }
+  if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
+    return MOE_LORA_ERR_MISALIGNED;
+  FusedArgs f = {};
+  f.x = x;
+  for (int s = 0; s < kMaxSlices; ++s) {
+    f.lora_a[s] = lora_a[s < num_slices ? s : 0];
+    f.lora_b[s] = lora_b[s < num_slices ? s : 0];
+  }
+  f.y = y;
+  f.topk_weights = topk_weights;
+  f.lora_ids = lora_ids;
+  f.adapter_enabled = adapter_enabled;
+  f.err = err_flag;
+  f.M = M;
+  f.topk = topk;
+  f.num_experts = num_experts;
+  f.K = K;
+  f.N = N;
+  f.rank = rank;
+  f.max_loras = max_loras;
+  f.num_active_loras = num_active_loras;
+  f.add_inputs = add_inputs ? 1 : 0;
+  f.num_slices = num_slices;
+  f.x_per_pair = x_per_pair ? 1 : 0;
+  f.ldy = ldy;
+  f.y_offset = y_offset;
+  *out = f;
+  return 0;
+}
+
 // The kernel a fused call runs.  AUTO takes the tensor-core kernel (when it
 // supports the sizes) for batches of at least 1024 pairs or when the adapter
 // bytes the call may touch, by the block bound, exceed 48 MB: there the
@@ -145,36 +240,20 @@ int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping, c
                             max_num_m_blocks))
     return st;
   if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_GLOBAL) return MOE_LORA_ERR_INVALID_ARG;
-  if (num_active_loras == 0) return MOE_LORA_OK;
-  if (!lora_ids || !sorted_token_ids || !expert_ids || !num_tokens_post_padded) return MOE_LORA_ERR_INVALID_ARG;
-  if (M > 0 && (!topk_ids || !token_lora_mapping)) return MOE_LORA_ERR_INVALID_ARG;
-  const int v = resolve_align_variant(M, topk, num_experts, variant);
-  if (v == MOE_LORA_ALIGN_SMEM && !align_smem_fits(num_experts)) return MOE_LORA_ERR_UNSUPPORTED;
-  DeviceInfo dev;
-  if (int st = current_device_info(&dev)) return st;
-  AlignArgs a;
-  a.topk_ids = topk_ids;
-  a.token_lora_mapping = token_lora_mapping;
-  a.lora_ids = lora_ids;
-  a.adapter_enabled = adapter_enabled;
-  a.sorted_token_ids = sorted_token_ids;
-  a.expert_ids = expert_ids;
-  a.num_tokens_post_padded = num_tokens_post_padded;
-  a.err = err_flag;
-  a.M = M;
-  a.topk = topk;
-  a.num_experts = num_experts;
-  a.max_loras = max_loras;
-  a.num_active_loras = num_active_loras;
-  a.block_size = block_size;
-  a.max_num_tokens_padded = max_num_tokens_padded;
-  a.max_num_m_blocks = max_num_m_blocks;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (v == MOE_LORA_ALIGN_SMEM) return launch_align_smem(a, s);
-  const size_t need = align_global_workspace_bytes(M, topk, num_experts, num_active_loras);
-  if (!workspace || workspace_bytes < need) return MOE_LORA_ERR_WORKSPACE;
-  if (!aligned16(workspace)) return MOE_LORA_ERR_MISALIGNED;
-  return launch_align_global(a, workspace, s);
+  if (M > 0 && num_active_loras > 0 && !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_active_loras > 0 && !lora_ids) return MOE_LORA_ERR_INVALID_ARG;
+  return align_impl(topk_ids, token_lora_mapping, lora_ids, adapter_enabled, M, topk, num_experts, max_loras,
+                    num_active_loras, block_size, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                    max_num_tokens_padded, max_num_m_blocks, workspace, workspace_bytes, variant, err_flag, stream);
+}
+
+int moe_align_block_size(const int32_t *topk_ids, int M, int topk, int num_experts, int block_size,
+                         int32_t *sorted_token_ids, int32_t *expert_ids, int32_t *num_tokens_post_padded,
+                         int max_num_tokens_padded, int max_num_m_blocks, void *workspace, size_t workspace_bytes,
+                         int variant, int32_t *err_flag, void *stream) {
+  return align_impl(topk_ids, nullptr, nullptr, nullptr, M, topk, num_experts, 1, 1, block_size, sorted_token_ids,
+                    expert_ids, num_tokens_post_padded, max_num_tokens_padded, max_num_m_blocks, workspace,
+                    workspace_bytes, variant, err_flag, stream);
 }
 
 int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
@@ -209,55 +288,23 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair, cons
   if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
                             max_num_m_blocks))
     return st;
-  if (K < 8 || N < 8 || rank < 1) return MOE_LORA_ERR_INVALID_ARG;
-  if (num_slices < 1 || num_slices > kMaxSlices || !lora_a || !lora_b) return MOE_LORA_ERR_INVALID_ARG;
-  if (y_offset < 0 || ldy < 8 || (long long)y_offset + (long long)num_slices * N > ldy) return MOE_LORA_ERR_INVALID_ARG;
-  if (rank > kMaxRank || rank % 4 != 0) return MOE_LORA_ERR_UNSUPPORTED;
-  if (K % 8 != 0 || N % 8 != 0 || ldy % 8 != 0 || y_offset % 8 != 0) return MOE_LORA_ERR_MISALIGNED;
   if (path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_CUDA_CORE_STREAM) return MOE_LORA_ERR_INVALID_ARG;
   if ((path == MOE_LORA_PATH_TCGEN05 || path == MOE_LORA_PATH_CUDA_CORE_STREAM) && rank % 8 != 0)
     return MOE_LORA_ERR_UNSUPPORTED;
-  const long long x_rows = x_per_pair ? (long long)M * topk : (long long)M;
-  if (x_rows * K > INT32_MAX * 8LL || (long long)M * topk * ldy > INT32_MAX * 8LL) return MOE_LORA_ERR_UNSUPPORTED;
-  if (num_active_loras == 0 || M == 0) return MOE_LORA_OK;
-  if (!x || !y || !sorted_token_ids || !expert_ids || !num_tokens_post_padded || !lora_ids)
-    return MOE_LORA_ERR_INVALID_ARG;
-  for (int s = 0; s < num_slices; ++s) {
-    if (!lora_a[s] || !lora_b[s]) return MOE_LORA_ERR_INVALID_ARG;
-    if (!aligned16(lora_a[s]) || !aligned16(lora_b[s])) return MOE_LORA_ERR_MISALIGNED;
-  }
-  if (!aligned16(x) || !aligned16(y) || (reinterpret_cast<uintptr_t>(topk_weights) & 3u))
-    return MOE_LORA_ERR_MISALIGNED;
   FusedArgs f;
-  f.x = x;
-  for (int s = 0; s < kMaxSlices; ++s) {
-    f.lora_a[s] = lora_a[s < num_slices ? s : 0];
-    f.lora_b[s] = lora_b[s < num_slices ? s : 0];
-  }
-  f.y = y;
-  f.topk_weights = topk_weights;
+  bool empty = false;
+  if (int st = prepare_fused(x, x_per_pair, lora_a, lora_b, num_slices, y, ldy, y_offset, topk_weights, lora_ids,
+                             adapter_enabled, M, topk, num_experts, K, N, rank, max_loras, num_active_loras,
+                             add_inputs, err_flag, &f, &empty))
+    return st;
+  if (empty) return MOE_LORA_OK;
+  if (!sorted_token_ids || !expert_ids || !num_tokens_post_padded) return MOE_LORA_ERR_INVALID_ARG;
   f.sorted_token_ids = sorted_token_ids;
   f.expert_ids = expert_ids;
   f.num_tokens_post_padded = num_tokens_post_padded;
-  f.lora_ids = lora_ids;
-  f.adapter_enabled = adapter_enabled;
-  f.err = err_flag;
-  f.M = M;
-  f.topk = topk;
-  f.num_experts = num_experts;
-  f.K = K;
-  f.N = N;
-  f.rank = rank;
-  f.max_loras = max_loras;
-  f.num_active_loras = num_active_loras;
   f.block_size = block_size;
   f.max_num_tokens_padded = max_num_tokens_padded;
   f.max_num_m_blocks = max_num_m_blocks;
-  f.add_inputs = add_inputs ? 1 : 0;
-  f.num_slices = num_slices;
-  f.x_per_pair = x_per_pair ? 1 : 0;
-  f.ldy = ldy;
-  f.y_offset = y_offset;
   const int use = resolve_path(f, path);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (use) {
@@ -265,6 +312,30 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair, cons
     case MOE_LORA_PATH_CUDA_CORE_STREAM: return launch_fused_stream_cc(f, s);
     default: return launch_fused_cuda_core(f, s);
   }
+}
+
+int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair, const moe_lora_bf16 *const *lora_a,
+                                       const moe_lora_bf16 *const *lora_b, int num_slices, moe_lora_bf16 *y,
+                                       int ldy, int y_offset, const float *topk_weights, const int32_t *topk_ids,
+                                       const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                                       const int32_t *adapter_enabled, int M, int topk, int num_experts, int K,
+                                       int N, int rank, int max_loras, int num_active_loras, int add_inputs,
+                                       int32_t *err_flag, void *stream) {
+  if (M < 0 || topk < 1 || num_experts < 1 || max_loras < 1 || num_active_loras < 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_experts > kMaxExperts || topk > num_experts) return MOE_LORA_ERR_UNSUPPORTED;
+  if (num_active_loras > max_loras) return MOE_LORA_ERR_INVALID_ARG;
+  if ((long long)M * topk > INT32_MAX / 2) return MOE_LORA_ERR_UNSUPPORTED;
+  FusedArgs f;
+  bool empty = false;
+  if (int st = prepare_fused(x, x_per_pair, lora_a, lora_b, num_slices, y, ldy, y_offset, topk_weights, lora_ids,
+                             adapter_enabled, M, topk, num_experts, K, N, rank, max_loras, num_active_loras,
+                             add_inputs, err_flag, &f, &empty))
+    return st;
+  if (empty) return MOE_LORA_OK;
+  if (!topk_ids || !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
+  f.topk_ids = topk_ids;
+  f.token_lora_mapping = token_lora_mapping;
+  return launch_fused_naive(f, static_cast<cudaStream_t>(stream));
 }
 
 int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a, const moe_lora_bf16 *lora_b,

@@ -87,8 +87,31 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const uint4 xv) {
   return s;
 }
 
+// Naive block assignment: whether pair f is covered, and its LoRA and
+// expert.  Uniform over the CTA (every thread returns the same), and over the
+// cluster (every CTA reads the same values).
+__device__ __forceinline__ bool naive_pair(const FusedArgs &p, int f, int &l, int &e) {
+  const int m = f / p.topk;
+  l = __ldg(p.token_lora_mapping + m);
+  e = __ldg(p.topk_ids + f);
+  const bool slot_ok = l >= 0 && l < p.max_loras && (!p.adapter_enabled || __ldg(p.adapter_enabled + l) != 0);
+  int listed = 0;
+  if (slot_ok)
+    for (int i = threadIdx.x; i < p.num_active_loras; i += blockDim.x) listed |= __ldg(p.lora_ids + i) == l;
+  listed = __syncthreads_or(listed);
+  if (!listed) return false;
+  if (e < 0 || e >= p.num_experts) {
+    if (threadIdx.x == 0 && cg::this_cluster().block_rank() == 0 && blockIdx.y == 0)
+      flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
+    return false;
+  }
+  return true;
+}
+
 // RV: elements of B per shared-memory vector (8 when rank % 8 == 0, else 4).
-template <int RV>
+// NAIVE: one pair per work item, found from topk_ids and token_lora_mapping
+// (naive block assignment, no align); otherwise blocks of the align output.
+template <int RV, bool NAIVE>
 __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedArgs p, const CcCfg cfg) {
   extern __shared__ __align__(128) uint8_t smem[];
   Meta &meta = *reinterpret_cast<Meta *>(smem);
@@ -105,26 +128,34 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int r = p.rank, K = p.K, N = p.N, E = p.num_experts, bs = p.block_size;
   const int P = p.M * p.topk;
-  const int z = blockIdx.y % p.num_active_loras;
-  const int sl = blockIdx.y / p.num_active_loras;   // adapter slice
+  // grid.y: slice * num_active_loras + slot (sorted), or the slice (naive)
+  const int z = NAIVE ? 0 : (int)(blockIdx.y % p.num_active_loras);
+  const int sl = NAIVE ? (int)blockIdx.y : (int)(blockIdx.y / p.num_active_loras);
 
-  // Uniform over the cluster: every CTA of it reads the same values.
-  const int l = __ldg(p.lora_ids + z);
-  if (l < 0 || l >= p.max_loras) {
-    if (c == 0 && tid == 0 && blockIdx.z == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
-    return;
+  wait_for_prior_grid();   // every input is read from here on
+  int l = 0, nitems = P, e_first = 0, f_first = -1;
+  if (!NAIVE) {
+    // Uniform over the cluster: every CTA of it reads the same values.
+    l = __ldg(p.lora_ids + z);
+    if (l < 0 || l >= p.max_loras) {
+      if (c == 0 && tid == 0 && blockIdx.z == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
+      return;
+    }
+    if (p.adapter_enabled && __ldg(p.adapter_enabled + l) == 0) return;
+    // The first block's expert and pair ids are requested together with the
+    // slot's block count (one round trip); they are only used if the block exists.
+    const int b_first = blockIdx.z;
+    e_first = __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b_first);
+    if (tid < bs && b_first * bs + tid < p.max_num_tokens_padded)
+      f_first = __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + b_first * bs + tid);
+    nitems = min(__ldg(p.num_tokens_post_padded + l) / bs, p.max_num_m_blocks);
+    if (b_first >= nitems) return;
+  } else if (c == 0 && tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+    for (int i = 0; i < p.num_active_loras; ++i) {
+      const int li = __ldg(p.lora_ids + i);
+      if (li < 0 || li >= p.max_loras) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
+    }
   }
-  if (p.adapter_enabled && __ldg(p.adapter_enabled + l) == 0) return;
-  wait_for_prior_grid();   // align outputs are read from here on
-  // The first block's expert and pair ids are requested together with the
-  // slot's block count (one round trip); they are only used if the block exists.
-  const int b_first = blockIdx.z;
-  const int e_first = __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b_first);
-  int f_first = -1;
-  if (tid < bs && b_first * bs + tid < p.max_num_tokens_padded)
-    f_first = __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + b_first * bs + tid);
-  const int nblocks = min(__ldg(p.num_tokens_post_padded + l) / bs, p.max_num_m_blocks);
-  if (b_first >= nblocks) return;
 
   if (tid == 0) {
     mbar_init(&meta.bar, 1);
@@ -141,14 +172,25 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
   const int n_lo = (c * n8 / C) * 8, n_hi = ((c + 1) * n8 / C) * 8;
   const int kn = k_hi - k_lo, nn = n_hi - n_lo;
 
-  for (int b = b_first; b < nblocks; b += gridDim.z) {
-    const int e = b == b_first ? e_first : __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b);
-    // Compact the block's real pairs, keeping their order.
-    {
+  for (int b = blockIdx.z; b < nitems; b += gridDim.z) {
+    int e;
+    if (NAIVE) {
+      // work item b is pair b
+      if (!naive_pair(p, b, l, e)) continue;
+      if (tid == 0) {
+        meta.pf[0] = b;
+        meta.pm[0] = x_row(p, b);
+        meta.pw[0] = route_weight(p, b);
+        meta.nv = 1;
+      }
+      __syncthreads();
+    } else {
+      e = b == (int)blockIdx.z ? e_first : __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b);
+      // Compact the block's real pairs, keeping their order.
       const int idx = b * bs + tid;
       int f = -1;
       if (tid < bs && idx < p.max_num_tokens_padded) {
-        f = b == b_first ? f_first : __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + idx);
+        f = b == (int)blockIdx.z ? f_first : __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + idx);
         if (f < 0 || f > P) {
           if (c == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
           f = -1;
@@ -173,10 +215,10 @@ __global__ void __launch_bounds__(kThreads) fused_cuda_core_kernel(const FusedAr
       }
       if (tid == 0) meta.nv = tot;
       __syncthreads();
-    }
-    if (e < 0 || e >= E) {  // uniform over the cluster
-      if (tid == 0 && c == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
-      continue;
+      if (e < 0 || e >= E) {  // uniform over the cluster
+        if (tid == 0 && c == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
+        continue;
+      }
     }
     const int nv = meta.nv;
     const size_t le = (size_t)l * E + e;
@@ -366,6 +408,42 @@ int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, CcCfg *cfg) {
 
 }  // namespace
 
+namespace {
+
+template <bool NAIVE>
+int launch_mode(const FusedArgs &f, const CcCfg &cfg, unsigned gy, unsigned gz, cudaStream_t stream) {
+  const void *fn = (f.rank % 8 == 0) ? (const void *)fused_cuda_core_kernel<8, NAIVE>
+                                     : (const void *)fused_cuda_core_kernel<4, NAIVE>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes) != cudaSuccess)
+    return MOE_LORA_ERR_LAUNCH;
+  if (cfg.C > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return MOE_LORA_ERR_LAUNCH;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(cfg.C, gy, gz);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = cfg.smem_bytes;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cfg.C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  // May start while the kernel before it (the align) is finishing: it waits
+  // for that kernel with griddepcontrol.wait before reading any input.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  cudaError_t err;
+  if (f.rank % 8 == 0)
+    err = cudaLaunchKernelEx(&lc, fused_cuda_core_kernel<8, NAIVE>, f, cfg);
+  else
+    err = cudaLaunchKernelEx(&lc, fused_cuda_core_kernel<4, NAIVE>, f, cfg);
+  return err == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
+}
+
+}  // namespace
+
 int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = current_device_info(&dev)) return st;
@@ -385,34 +463,22 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   if (per_slot > cap) per_slot = cap;
   if (per_slot > 65535) per_slot = 65535;
   if (per_slot <= 0) return 0;
-  const void *fn = (f.rank % 8 == 0) ? (const void *)fused_cuda_core_kernel<8>
-                                     : (const void *)fused_cuda_core_kernel<4>;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes) != cudaSuccess)
-    return MOE_LORA_ERR_LAUNCH;
-  if (cfg.C > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
-    return MOE_LORA_ERR_LAUNCH;
-  cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(cfg.C, f.num_active_loras * f.num_slices, (unsigned)per_slot);
-  lc.blockDim = dim3(kThreads, 1, 1);
-  lc.dynamicSmemBytes = cfg.smem_bytes;
-  lc.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cfg.C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  // May start while the align kernel before it is finishing (it waits for it
-  // with griddepcontrol.wait before touching the align outputs).
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  lc.attrs = attr;
-  lc.numAttrs = 2;
-  cudaError_t err;
-  if (f.rank % 8 == 0)
-    err = cudaLaunchKernelEx(&lc, fused_cuda_core_kernel<8>, f, cfg);
-  else
-    err = cudaLaunchKernelEx(&lc, fused_cuda_core_kernel<4>, f, cfg);
-  return err == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
+  return launch_mode<false>(f, cfg, (unsigned)(f.num_active_loras * f.num_slices), (unsigned)per_slot, stream);
+}
+
+int launch_fused_naive(const FusedArgs &f, cudaStream_t stream) {
+  DeviceInfo dev;
+  if (int st = current_device_info(&dev)) return st;
+  CcCfg cfg;
+  if (int st = pick_cfg(f, dev, &cfg)) return st;
+  // grid (C, slices, pairs), as the one-program-per-pair grid of the naive
+  // assignment; past a few waves, CTAs walk several pairs.
+  long long items = (long long)f.M * f.topk;
+  const long long cap = std::max<long long>(64, 16LL * dev.sm_count / ((long long)cfg.C * f.num_slices));
+  if (items > cap) items = cap;
+  if (items > 65535) items = 65535;
+  if (items <= 0) return 0;
+  return launch_mode<true>(f, cfg, (unsigned)f.num_slices, (unsigned)items, stream);
 }
 
 }  // namespace moe_lora

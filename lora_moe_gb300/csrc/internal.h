@@ -11,8 +11,8 @@ namespace moe_lora {
 // Align outputs and inputs, as validated by the C-ABI layer.
 struct AlignArgs {
   const int32_t *topk_ids;
-  const int32_t *token_lora_mapping;
-  const int32_t *lora_ids;
+  const int32_t *token_lora_mapping;  // null: every token in the one slot (plain MoE align)
+  const int32_t *lora_ids;            // null: slot z is row z
   const int32_t *adapter_enabled;  // may be null
   int32_t *sorted_token_ids;
   int32_t *expert_ids;
@@ -31,9 +31,11 @@ struct FusedArgs {
   const uint16_t *lora_b[kMaxSlices];  // per slice: bf16 [L, E, N, r]
   uint16_t *y;                         // bf16 [M, topk, ldy]; slice s at columns y_offset + s*N
   const float *topk_weights;           // fp32 [M, topk] or null (no router-weight scaling)
-  const int32_t *sorted_token_ids;
+  const int32_t *sorted_token_ids;        // align outputs (null for naive block assignment)
   const int32_t *expert_ids;
   const int32_t *num_tokens_post_padded;
+  const int32_t *topk_ids;                // routing (naive block assignment only)
+  const int32_t *token_lora_mapping;
   const int32_t *lora_ids;
   const int32_t *adapter_enabled;  // may be null
   int32_t *err;                    // may be null
@@ -83,6 +85,8 @@ bool align_smem_fits(int E);
 int launch_align_smem(const AlignArgs &a, cudaStream_t stream);
 int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream);
 int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream);
+// Naive block assignment: one work item per pair, no align outputs.
+int launch_fused_naive(const FusedArgs &f, cudaStream_t stream);
 int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream);
 // Whether the tensor-core path takes these arguments (rank % 8 == 0, at most
 // 128 listed slots).

@@ -95,6 +95,19 @@ def align(topk_ids, token_lora_mapping, lora_ids, num_experts, max_loras, block_
     return st, sorted_ids, expert_ids, ntpp
 
 
+def align_plain(topk_ids, num_experts, block_size, max_num_tokens_padded=None, max_num_m_blocks=None,
+                fill=-7):
+    """The plain (non-LoRA) MoE align: the single-slot case of align(), every
+    token owned by slot 0.
+
+    Returns (status, sorted_token_ids [cap], expert_ids [capb], ntpp [1])."""
+    topk_ids = _c32(topk_ids)
+    M = topk_ids.shape[0]
+    st, s, e, n = align(topk_ids, np.zeros(M, np.int32), np.array([0], np.int32), num_experts, 1, block_size,
+                        max_num_tokens_padded=max_num_tokens_padded, max_num_m_blocks=max_num_m_blocks, fill=fill)
+    return st, s[0], e[0], n
+
+
 def fused(x, lora_a, lora_b, y_in, topk_ids, token_lora_mapping, lora_ids,
           add_inputs=True, adapter_enabled=None):
     """Run the fused oracle over every pair.  Returns float64 [M, topk, N]."""

@@ -157,3 +157,35 @@ def test_fused_resolve_path():
     assert R(16, 8, 128, 2048, 1536, 12, 2, 16, 1, 2) == -2  # tensor cores need rank % 8 == 0
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 5, 0) == -1  # too many slices
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 9) == -1
+
+
+def test_plain_align_argument_errors():
+    f = B.lib().moe_align_block_size
+    # (topk_ids, M, topk, E, bs, sorted, experts, ntpp, cap, capb, ws, ws_bytes, variant, err, stream)
+    assert f(None, 16, 2, 1025, 16, None, None, None, 10000, 1000, None, 0, 0, None, None) == 2
+    assert f(None, 16, 2, 8, 8, None, None, None, 10000, 1000, None, 0, 0, None, None) == 2
+    assert f(None, 16, 2, 8, 16, None, None, None, 10, 1, None, 0, 0, None, None) == 1     # capacity too small
+    assert f(None, 16, 2, 8, 16, None, None, None, 152, 10, None, 0, 7, None, None) == 1   # bad variant
+    assert f(None, 16, 2, 8, 16, None, None, None, 152, 10, None, 0, 0, None, None) == 1   # NULL buffers
+    assert B.align_workspace_bytes(4096, 8, 256, 1, 64, B.ALIGN_GLOBAL) > 0
+
+
+def test_fused_naive_argument_errors():
+    P = ctypes.c_void_p
+
+    def naive(slices=1, **kw):
+        args = dict(x=None, x_per_pair=0, a=(P * max(slices, 1))(), b=(P * max(slices, 1))(), S=slices, y=None,
+                    ldy=512, y_off=0, w=None, topk_ids=None, mapping=None, lora_ids=None, enabled=None, M=16,
+                    topk=2, E=8, K=256, N=512, r=8, L=2, nact=2, add=1, err=None, stream=None)
+        args.update(kw)
+        return B.lib().moe_lora_fused_shrink_expand_naive(*args.values())
+
+    assert naive(E=1025) == 2
+    assert naive(topk=9) == 2
+    assert naive(nact=3) == 1
+    assert naive(r=132) == 2
+    assert naive(K=260) == 3
+    assert naive(slices=0) == 1
+    assert naive(nact=0) == 0          # zero grid
+    assert naive(M=0) == 0
+    assert naive() == 1                # NULL buffers

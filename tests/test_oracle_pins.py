@@ -194,6 +194,30 @@ def test_align_single_lora_is_plain_moe_align():
     assert list(s[0, :n[0]]) == seq and list(e[0, :n[0] // bs]) == blocks
 
 
+@pytest.mark.parametrize("seed,M,topk,E,bs", [(1, 50, 4, 16, 8), (2, 3, 1, 1, 16), (3, 200, 8, 64, 64),
+                                               (4, 0, 2, 4, 16), (5, 33, 6, 6, 128)])
+def test_align_plain_is_stable_sort_by_expert(seed, M, topk, E, bs):
+    """The plain align (no LoRA): a stable sort of all pairs by expert
+    (numpy argsort, kind='stable'), padded per expert to block_size with the
+    sentinel M*topk; experts without pairs get no block."""
+    rng = np.random.default_rng(seed)
+    topk_ids = rng.integers(0, E, size=(M, topk)).astype(np.int32)
+    st, s, e, n = oracle.align_plain(topk_ids, E, bs)
+    order = np.argsort(topk_ids.ravel(), kind="stable")
+    keys = topk_ids.ravel()[order]
+    seq, blocks = [], []
+    for ex in range(E):
+        fs = order[keys == ex]
+        if len(fs) == 0:
+            continue
+        nb = -(-len(fs) // bs)
+        seq += list(fs) + [M * topk] * (nb * bs - len(fs))
+        blocks += [ex] * nb
+    assert st == 0 and n[0] == len(seq)
+    assert list(s[:n[0]]) == seq and list(e[:n[0] // bs]) == blocks
+    assert (s[n[0]:] == -7).all() and (e[n[0] // bs:] == -7).all()
+
+
 def test_align_reports_bad_ids():
     topk_ids = np.array([[0, 5], [1, 2]], np.int32)   # 5 is out of range for E=3
     st, s, e, n = oracle.align(topk_ids, np.array([0, 0], np.int32), np.array([0], np.int32), 3, 1, 2)
