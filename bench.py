@@ -423,7 +423,7 @@ def run_ours(args, world, rank, local, pg):
                     lora_ids=torch.from_numpy(inp.lora_ids).pin_memory(),
                     x=torch.from_numpy(src.x.view(np.int16)).pin_memory(),
                     y=torch.from_numpy(src.y_in.view(np.int16)).pin_memory())
-        if "w" in base:
+        if "w" in sets[0]:
             host["w"] = torch.from_numpy(ex.topk_weights).pin_memory()
         out_host = torch.empty(src.y_in.shape, dtype=torch.int16).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())

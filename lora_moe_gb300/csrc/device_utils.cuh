@@ -152,6 +152,19 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Cluster barrier halves.  arrive.release orders this thread's earlier memory
+// operations (its shared-memory writes that peers will read) before the
+// barrier; arrive.relaxed orders nothing, so it does not wait for earlier
+// global stores to drain.  wait.acquire makes what peers released visible.
+// Executed by every thread of the CTA (aligned forms).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
 // Programmatic dependent launch: wait until the preceding grid in the stream
 // (the align kernel) has completed and its writes are visible.  A no-op when
 // the kernel was not launched as a dependent.

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&meta.full_ex[s], 1 + 32);
       mbar_init(&meta.empty_ex[s], 1 + kEpiWarps / 2);   // MMA commit + the 4 warps of one group
     }
-    for (int a = 0; a < 4; ++a) {
+    for (int a = 0; a < 2; ++a) {
       mbar_init(&meta.tfull[a], 1);
       mbar_init(&meta.tempty[a], kEpiWarps / 2);       // accumulator a is drained by group a % 2
     }
@@ -182,7 +182,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3, h = (warp - 2) >> 2;
     const int etid = tid - 64;
     const int gtid = etid & 127;             // thread index inside the group
-    constexpr int kCR = BS < 32 ? BS : 32;   // rows per piece of a tile
+    // rows per piece of a tile: 16 keeps the live values per thread low
+    // enough that the epilogue's schedule does not depend on small changes
+    // elsewhere in the kernel (32-row pieces ran 10-15% slower after an
+    // unrelated change to the argument block)
+    constexpr int kCR = BS < 16 ? BS : 16;
     constexpr int kChunks = BS / kCR;
     constexpr int kStoreRows = BS / 8;       // rows a thread stores per tile
     uint32_t ex_iter = 0, acc_iter = 0;
@@ -371,7 +375,7 @@ int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream_) {
     if (int st = stream::plan(f, dev, 2 * part, 2, &cfg)) return st;
     cfg.t_part = part;   // the kernel addresses T buffers as [t_bufs][hi, lo] of one part each
   }
-  cfg.nacc = 2;
+  cfg.nacc = 2;   // Meta holds barriers for two expand accumulators
   int cols = 32;
   while (cols < cfg.nacc * f.block_size + cfg.r_pad) cols <<= 1;
   cfg.tmem_cols = cols;

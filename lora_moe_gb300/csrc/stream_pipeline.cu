@@ -79,7 +79,8 @@ int plan(const FusedArgs &f, const DeviceInfo &dev, int consumer_bytes, int t_bu
   cfg->yt_off = round_up(cfg->natoms * kTileN * kb, 1024);
   cfg->ex_stage = round_up(cfg->yt_off + BS * kTileN * 2, 1024);
   cfg->t_part = round_up(consumer_bytes, 1024);
-  const int meta_bytes = round_up((int)sizeof(Meta), 1024);
+  // The Meta block sits last and needs no more than 16-byte alignment.
+  const int meta_bytes = round_up((int)sizeof(Meta), 128);
   const int budget = (int)dev.max_smem_optin;
 
   // Choose the ring depths with the most bytes in flight (the shrink ring has
@@ -100,8 +101,10 @@ int plan(const FusedArgs &f, const DeviceInfo &dev, int consumer_bytes, int t_bu
         // the M=128 shrink MMA of the tensor-core kernel reads 128 x-tile rows:
         // the rows past block_size (never used) must still lie in the allocation
         if (cfg->sh_stage + after_sh < 128 * 128) continue;
+        // a one-stage expand ring cannot load the next tile while the current
+        // one is in use: taken only when no deeper ring fits
         const int score = std::min(sh_fly, 128 * 1024) + std::min(s_ex * cfg->ex_stage, 128 * 1024) +
-                          (t_bufs == 2 ? 8 * 1024 : 0) - total / 64;
+                          (t_bufs == 2 ? 8 * 1024 : 0) - total / 64 - (s_ex == 1 ? (1 << 24) : 0);
         if (score > best) {
           best = score;
           found = true;

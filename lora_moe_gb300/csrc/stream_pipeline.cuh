@@ -65,7 +65,7 @@ struct TmapSet {
 struct Meta {
   uint64_t full_sh[kMaxStages], empty_sh[kMaxStages];
   uint64_t full_ex[kMaxStages], empty_ex[kMaxStages];
-  uint64_t tfull[4], tempty[4];
+  uint64_t tfull[2], tempty[2];   // (tensor-core kernel) the two expand accumulators
   uint64_t shrink_done, shrink_free;
   uint64_t t_full[2], t_empty[2];
   uint32_t tmem_base;
@@ -76,7 +76,7 @@ struct Meta {
   int epi_f[128];     // consumers' copy
   float epi_w[128];   // consumers: router weight of each row's pair
   int cpx[128];       // consumers: rows (positions in the block) of the real pairs, in order
-  int wcount[16];
+  int wcount[8];      // (CUDA-core kernel) real pairs per compute warp
 };
 
 // Shared-memory descriptor of a K-major operand tile whose rows are
