@@ -116,6 +116,16 @@ def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weigh
                 align_bytes=align_bytes, flops=2 * r * (w.K + w.N) * P * slices)
 
 
+# DRAM bytes per launch of the dominant kernel (dram__bytes_read.sum +
+# dram__bytes_write.sum) from one ncu capture of the plain call, by workload
+# and kernel; profiles/ holds each capture's summary and command.  An entry
+# must go when its kernel changes.
+NCU_TRAFFIC = {
+    ("decode_qwen3_w13", "fused_cuda_core_kernel"): 5573632,      # fused_cuda_core_decode_qwen3_w13.md
+    ("decode_gptoss_w2", "fused_tcgen05_kernel"): 171245568,      # fused_tcgen05_decode_gptoss_w2.md
+}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -557,7 +567,8 @@ def main():
         "roofline": {"bound": "hbm", "kernel": res["kernel_name"], "achieved": res["achieved"], "peak": res["peak"],
                      "unit": "GB/s",
                      "frac": res["achieved"] / res["peak"], "peak_kind": res["peak_kind"] + " (hbm_gbs)",
-                     "traffic": None},
+                     "traffic": None if uses_ex(args) else NCU_TRAFFIC.get((w.name, res["kernel_name"])),
+                     "traffic_unit": "bytes per launch (ncu)"},
         "cpu_baseline": cpu,
         "e2e": res["e2e"],
         "gpu_launches": args.steps * (res["align_launches"] + 1),
