@@ -225,6 +225,13 @@ def max_over_ranks(pg, value, use_cuda):
     return float(t.item())
 
 
+def job_us_per_step(pg, ms_local, steps, world, use_cuda):
+    """Whole-job microseconds per step: the slowest rank's time for its
+    `steps` steps, over all ranks' steps (each rank runs its own replica)."""
+    ms = max_over_ranks(pg, ms_local, use_cuda)
+    return ms * 1e3 / (steps * world), ms
+
+
 # --------------------------------------------------------------------------- CPU oracle timing
 
 def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: int = None, ex=None,
@@ -395,8 +402,7 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
     barrier(pg, True)
     clocks = sampler.stop()
-    ms = e0.elapsed_time(e1)
-    ms = max_over_ranks(pg, ms, True)
+    _, ms = job_us_per_step(pg, e0.elapsed_time(e1), args.steps, world, True)
     assert int(err.item()) == 0, "device error flag %d" % int(err.item())
 
     # ---------------- kernel-level timing (each kernel alone, same rotation)
