@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   wait_for_prior_grid();   // align outputs are read from here on
   stream::slot_prefix<BS>(p, meta);
   __syncthreads();
-  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, p.num_slices, cfg.nt_total);
+  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, p.num_slices, cfg);
 
   if (warp == 9 || warp == 10) {
     stream::shrink_producer<BS>(p, cfg, meta, &maps, sh_base, rg, warp - 9);

@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *t_base = smem + cfg.off_t;
   const int N = p.N, E = p.num_experts, r = p.rank, r_pad = cfg.r_pad;
   const int P = p.M * p.topk;
-  const int kt_total = cfg.kt_total, nt_total = cfg.nt_total;
+  const int kt_total = cfg.kt_total;
   const int kb = cfg.ka * 2;     // bytes per expand-operand row per atom
   volatile int *abort = &meta.abort;
 
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = meta.tmem_base;
   const uint32_t tmem_sh = tmem + cfg.nacc * BS;   // shrink accumulator columns
 
-  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, p.num_slices, nt_total);
+  const stream::Range rg = stream::cta_range(meta, p.num_active_loras, p.num_slices, cfg);
   const int gb0 = rg.gb0, gb1 = rg.gb1;
   auto tile_lo = [&](int gb) { return rg.tile_lo(gb); };
   auto tile_hi = [&](int gb) { return rg.tile_hi(gb); };

@@ -79,6 +79,8 @@ int plan(const FusedArgs &f, const DeviceInfo &dev, int consumer_bytes, int t_bu
   cfg->yt_off = round_up(cfg->natoms * kTileN * kb, 1024);
   cfg->ex_stage = round_up(cfg->yt_off + BS * kTileN * 2, 1024);
   cfg->t_part = round_up(consumer_bytes, 1024);
+  cfg->unit_sh_bytes = (long long)cfg->kt_total * (BS * 128 + cfg->r_pad * 128);
+  cfg->tile_bytes = (long long)cfg->natoms * kTileN * kb + (long long)BS * kTileN * 2;
   // The Meta block sits last and needs no more than 16-byte alignment.
   const int meta_bytes = round_up((int)sizeof(Meta), 128);
   const int budget = (int)dev.max_smem_optin;

@@ -54,6 +54,8 @@ struct Cfg {
   int off_meta;
   int smem_bytes;
   int kt_total, nt_total;
+  long long unit_sh_bytes;   // bytes one unit's shrink streams (x rows + A, all k-tiles)
+  long long tile_bytes;      // bytes one expand tile streams (B tile + y_in rows)
 };
 
 // The A and B tensor maps of every slice (kernel parameter).
@@ -153,11 +155,26 @@ struct Range {
   __device__ int tile_hi(int gb) const { return (int)min(t1 - (long long)gb * nt_total, (long long)nt_total); }
 };
 
-__device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int num_slices, int nt_total) {
+// Two ways to split the list: equal shares of (unit, tile) pairs, where a
+// unit cut by a share boundary has its shrink streamed by both CTAs, or whole
+// units, at most ceil(units / CTAs) each.  Every CTA takes the one whose
+// busiest CTA streams fewer bytes (the same choice everywhere: it depends on
+// the unit count, the grid and the configuration only).
+__device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int num_slices, const Cfg &cfg) {
   Range rg;
-  const long long total = (long long)meta.prefix[nact] * num_slices * nt_total;
-  rg.t0 = total * blockIdx.x / gridDim.x;
-  rg.t1 = total * (blockIdx.x + 1) / gridDim.x;
+  const int nt_total = cfg.nt_total;
+  const long long units = (long long)meta.prefix[nact] * num_slices;
+  const long long total = units * nt_total;
+  const double per = (double)units / gridDim.x;
+  const double shared_cost = (per + 1.0) * (double)cfg.unit_sh_bytes + per * nt_total * (double)cfg.tile_bytes;
+  const double whole_cost = ceil(per) * ((double)cfg.unit_sh_bytes + nt_total * (double)cfg.tile_bytes);
+  if (whole_cost < shared_cost) {
+    rg.t0 = units * blockIdx.x / gridDim.x * nt_total;
+    rg.t1 = units * (blockIdx.x + 1) / gridDim.x * nt_total;
+  } else {
+    rg.t0 = total * blockIdx.x / gridDim.x;
+    rg.t1 = total * (blockIdx.x + 1) / gridDim.x;
+  }
   rg.nt_total = nt_total;
   rg.gb0 = (int)(rg.t0 / nt_total);
   rg.gb1 = rg.t1 > rg.t0 ? (int)((rg.t1 - 1) / nt_total) : rg.gb0 - 1;
