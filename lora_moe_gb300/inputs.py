@@ -94,6 +94,18 @@ WORKLOADS = {
     "large_e_nact8": Workload("large_e_nact8", M=4096, K=7168, N=4096, E=256, topk=8,
                               max_loras=8, num_active_loras=8, rank=128, block_size=64,
                               mapping="uniform_with_none", experts="zipf", zipf_s=1.2),
+    # Profiling-sized cases.  A full ncu capture replays each launch dozens of
+    # times and saves device memory between replays, so it runs on inputs of a
+    # few GB at most: the prefill shape at a quarter of the tokens (y still
+    # larger than L2), and the rank-128 large-E shape with one adapter slot
+    # allocated (the same active work as large_e_nact1 without the 5 GB of
+    # inactive slots).
+    "prefill_mixtral_w13_m2048": Workload("prefill_mixtral_w13_m2048", M=2048, K=4096, N=28672, E=8, topk=2,
+                                          max_loras=4, num_active_loras=4, rank=16, block_size=64,
+                                          mapping="uniform", experts="uniform"),
+    "large_e_l1": Workload("large_e_l1", M=4096, K=7168, N=4096, E=256, topk=8, max_loras=1,
+                           num_active_loras=1, rank=128, block_size=64, mapping="uniform_with_none",
+                           experts="zipf", zipf_s=1.2),
 }
 
 
