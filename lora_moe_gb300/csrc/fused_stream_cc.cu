@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = p.N, E = p.num_experts, r = p.rank, r_pad = cfg.r_pad, P = p.M * p.topk;
     const int kb = cfg.ka * 2;
     uint32_t sh_iter = 0, ex_iter = 0;
-    for (int gb = rg.gb0; gb <= rg.gb1; ++gb) {
+    for (int gb = rg.gb0; gb <= rg.gb1; gb += rg.step) {
       const stream::BlockRef br = stream::block_ref<BS>(p, meta, gb);
       const bool e_ok = br.e >= 0 && br.e < E;
       // -- the block's real pairs, in order: row in the block and pair id

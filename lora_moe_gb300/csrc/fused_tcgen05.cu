@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = make_idesc_bf16(kMmaRows, r_pad);
       uint32_t sh_iter = 0;
       int kk = 0;
-      for (int gb = gb0; gb <= gb1; ++gb, ++kk) {
+      for (int gb = gb0; gb <= gb1; gb += rg.step, ++kk) {
         if (kk > 0) mbar_wait(&meta.shrink_free, (kk - 1) & 1, abort, p.err);
         tc_fence_after();
         for (int kt = 0; kt < kt_total; ++kt, ++sh_iter) {
@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc = make_idesc_bf16(kMmaRows, BS);
       uint32_t ex_iter = 0, acc_iter = 0;
       int kk = 0;
-      for (int gb = gb0; gb <= gb1; ++gb, ++kk) {
+      for (int gb = gb0; gb <= gb1; gb += rg.step, ++kk) {
         const int tb = kk % cfg.t_bufs;
         mbar_wait(&meta.t_full[tb], (kk / cfg.t_bufs) & 1, abort, p.err);
         tc_fence_after();
@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kStoreRows = BS / 8;       // rows a thread stores per tile
     uint32_t ex_iter = 0, acc_iter = 0;
     int kk = 0;
-    for (int gb = gb0; gb <= gb1; ++gb, ++kk) {
+    for (int gb = gb0; gb <= gb1; gb += rg.step, ++kk) {
       const stream::BlockRef br = stream::block_ref<BS>(p, meta, gb);
       const bool e_ok = br.e >= 0 && br.e < E;
       named_barrier(1, kEpiThreads);   // every epilogue thread is done with the previous block's epi_f

@@ -149,7 +149,7 @@ __device__ __forceinline__ void slot_prefix(const FusedArgs &p, Meta &meta) {
 // (gb0..gb1 number units).
 struct Range {
   long long t0, t1;
-  int gb0, gb1;
+  int gb0, gb1, step;   // units gb0, gb0 + step, ..., gb1
   int nt_total;
   __device__ int tile_lo(int gb) const { return (int)max(t0 - (long long)gb * nt_total, 0LL); }
   __device__ int tile_hi(int gb) const { return (int)min(t1 - (long long)gb * nt_total, (long long)nt_total); }
@@ -169,12 +169,21 @@ __device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int num_s
   const double shared_cost = (per + 1.0) * (double)cfg.unit_sh_bytes + per * nt_total * (double)cfg.tile_bytes;
   const double whole_cost = ceil(per) * ((double)cfg.unit_sh_bytes + nt_total * (double)cfg.tile_bytes);
   if (whole_cost < shared_cost) {
-    rg.t0 = units * blockIdx.x / gridDim.x * nt_total;
-    rg.t1 = units * (blockIdx.x + 1) / gridDim.x * nt_total;
-  } else {
-    rg.t0 = total * blockIdx.x / gridDim.x;
-    rg.t1 = total * (blockIdx.x + 1) / gridDim.x;
+    // Whole units, strided over the grid: units u = blockIdx.x + i * gridDim.x.
+    // Consecutive units (the blocks of one segment share its A and B) run on
+    // neighbouring CTAs at the same time, so the later reads come from L2.
+    rg.t0 = 0;
+    rg.t1 = total;
+    rg.nt_total = nt_total;
+    rg.step = gridDim.x;
+    rg.gb0 = blockIdx.x;
+    rg.gb1 = units > blockIdx.x ? (int)(blockIdx.x + (units - 1 - blockIdx.x) / gridDim.x * gridDim.x)
+                                : rg.gb0 - rg.step;
+    return rg;
   }
+  rg.t0 = total * blockIdx.x / gridDim.x;
+  rg.t1 = total * (blockIdx.x + 1) / gridDim.x;
+  rg.step = 1;
   rg.nt_total = nt_total;
   rg.gb0 = (int)(rg.t0 / nt_total);
   rg.gb1 = rg.t1 > rg.t0 ? (int)((rg.t1 - 1) / nt_total) : rg.gb0 - 1;
@@ -196,7 +205,7 @@ __device__ void shrink_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, 
   const int ch = lane & 7;
   uint32_t sh_iter = 0;
   int owned = 0;
-  for (int gb = rg.gb0; gb <= rg.gb1; ++gb) {
+  for (int gb = rg.gb0; gb <= rg.gb1; gb += rg.step) {
     const BlockRef br = block_ref<BS>(p, meta, gb);
     const bool e_ok = br.e >= 0 && br.e < E;
     if (!e_ok && lane == 0 && me == 0) flag_error(p.err, MOE_LORA_DEVERR_EXPERT_ID);
@@ -260,7 +269,7 @@ __device__ void expand_producer(const FusedArgs &p, const Cfg &cfg, Meta &meta, 
   const int kb = cfg.ka * 2;
   volatile int *abort = &meta.abort;
   uint32_t ex_iter = 0;
-  for (int gb = rg.gb0; gb <= rg.gb1; ++gb) {
+  for (int gb = rg.gb0; gb <= rg.gb1; gb += rg.step) {
     const BlockRef br = block_ref<BS>(p, meta, gb);
     const int le = br.l * E + ((br.e >= 0 && br.e < E) ? br.e : 0);
     const CUtensorMap *tmap_b = &maps->b[br.s];
