@@ -159,7 +159,9 @@ struct Range {
 // unit cut by a share boundary has its shrink streamed by both CTAs, or whole
 // units, at most ceil(units / CTAs) each.  Every CTA takes the one whose
 // busiest CTA streams fewer bytes (the same choice everywhere: it depends on
-// the unit count, the grid and the configuration only).
+// the unit count, the grid and the configuration only).  Whole units are
+// strided over the grid, so units of one segment share their adapter reads
+// through L2, which the byte count leaves out: they are taken within 3%.
 __device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int num_slices, const Cfg &cfg) {
   Range rg;
   const int nt_total = cfg.nt_total;
@@ -168,7 +170,7 @@ __device__ __forceinline__ Range cta_range(const Meta &meta, int nact, int num_s
   const double per = (double)units / gridDim.x;
   const double shared_cost = (per + 1.0) * (double)cfg.unit_sh_bytes + per * nt_total * (double)cfg.tile_bytes;
   const double whole_cost = ceil(per) * ((double)cfg.unit_sh_bytes + nt_total * (double)cfg.tile_bytes);
-  if (whole_cost < shared_cost) {
+  if (whole_cost < 1.03 * shared_cost) {
     // Whole units, strided over the grid: units u = blockIdx.x + i * gridDim.x.
     // Consecutive units (the blocks of one segment share its A and B) run on
     // neighbouring CTAs at the same time, so the later reads come from L2.
