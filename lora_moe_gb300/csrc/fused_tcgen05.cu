@@ -11,10 +11,11 @@
 //
 // Work split.  The work of a call is the list of (unit, 128-column tile)
 // pairs, a unit being one adapter slice of one block of a listed slot (vLLM
-// PR #32005: the grid is sized by the active LoRAs).  Each persistent CTA takes
-// one contiguous, equal share of that list, so every SM streams the same
-// number of output tiles; a unit whose tiles straddle two CTAs has its shrink
-// computed by both.  T lives only in shared and tensor memory.
+// PR #32005: the grid is sized by the active LoRAs).  The persistent CTAs split
+// it either into equal shares of (unit, tile) pairs (a unit whose tiles
+// straddle two CTAs has its shrink computed by both) or into whole units
+// strided over the grid, whichever streams fewer bytes on the busiest CTA
+// (stream_pipeline.cuh, cta_range).  T lives only in shared and tensor memory.
 //
 // Warp roles (416 threads):
 //   warps 10, 11  shrink producers: alternate k-tiles; gather the block's x rows

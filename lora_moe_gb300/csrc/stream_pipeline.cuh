@@ -8,9 +8,10 @@
 // active LoRAs) and all adapter slices.  A (block, slice) pair is a "unit";
 // units are numbered block-major (unit = block * num_slices + slice) so that
 // the slices of one block, which gather the same x rows, run back to back.
-// Each persistent CTA takes one contiguous, equal share of that list.  For
-// every unit it touches it needs that unit's rank-r intermediate (the shrink
-// over all of K), then it produces its tiles of the unit.
+// Each persistent CTA takes a share of that list (cta_range: equal shares of
+// (unit, tile) pairs, or whole units strided over the grid).  For every unit
+// it touches it needs that unit's rank-r intermediate (the shrink over all of
+// K), then it produces its tiles of the unit.
 //
 // Two producers feed the consumers through shared-memory rings guarded by
 // mbarriers:
