@@ -301,6 +301,29 @@ int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair,
 int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank,
                                 int num_active_loras, int block_size, int num_slices, int path);
 
+/*
+ * moe_lora_fused_plan -- the launch plan a plain fused call with these sizes
+ * would use on a device with `sm_count` SMs and `max_smem_per_block` bytes of
+ * opt-in shared memory per block.  Host arithmetic only; no device is
+ * touched.  For inspection and tests.
+ *
+ *   out  [host] int32 [11]: kernel (MOE_LORA_PATH_TCGEN05 or
+ *        MOE_LORA_PATH_CUDA_CORE_CLUSTER), grid (0 for the cluster kernel:
+ *        capped at run time by the clusters that can be resident at once),
+ *        threads per CTA, dynamic shared memory bytes, then for the tensor-core
+ *        kernel the shrink ring depth, the shrink producers' lag, the expand
+ *        ring depth, the T buffers and the TMEM columns, and for the cluster
+ *        kernel the CTAs per cluster and the pairs per group (block_size for
+ *        the tensor-core kernel).
+ * Returns a moe_lora_status code (MOE_LORA_ERR_UNSUPPORTED for the CUDA-core
+ * streaming kernel, which has no plan here).  On a GB300 every tensor-core
+ * plan has at least two expand stages except block_size 128 with rank > 64,
+ * where only one fits beside the shrink stages and the T buffer.
+ */
+int moe_lora_fused_plan(int M, int topk, int num_experts, int K, int N, int rank,
+                        int num_active_loras, int block_size, int num_slices, int path,
+                        int sm_count, int max_smem_per_block, int32_t *out);
+
 /* Size of the scratch buffer built into the library for
  * moe_lora_align_static_workspace (4 MiB). */
 #define MOE_LORA_STATIC_WORKSPACE_BYTES ((size_t)4 << 20)

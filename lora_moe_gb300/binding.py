@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_fused_shrink_expand_naive.restype = I
             L.moe_lora_fused_shrink_expand_naive.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P), I, P, I, I,
                                                              P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
+            L.moe_lora_fused_plan.restype = I
+            L.moe_lora_fused_plan.argtypes = [I] * 12 + [P]
             L.moe_lora_fused_resolve_path.restype = I
             L.moe_lora_fused_resolve_path.argtypes = [I] * 10
             _lib = L
@@ -202,6 +204,21 @@ def fused_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, block
     if v < 0:
         raise MoeLoraError(-v, "moe_lora_fused_resolve_path")
     return v
+
+
+PLAN_FIELDS = ("kernel", "grid", "threads", "smem_bytes", "s_sh", "lag", "s_ex", "t_bufs", "tmem_cols", "cluster",
+               "pairs_per_group")
+
+
+def fused_plan(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices=1, path=PATH_AUTO,
+               sm_count=152, max_smem_per_block=232448) -> dict:
+    """The launch plan a plain fused call would use on a device with these
+    properties (host arithmetic only)."""
+    out = (ctypes.c_int32 * len(PLAN_FIELDS))()
+    st = lib().moe_lora_fused_plan(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices, path,
+                                   sm_count, max_smem_per_block, ctypes.cast(out, ctypes.c_void_p))
+    _check(st, "moe_lora_fused_plan")
+    return dict(zip(PLAN_FIELDS, list(out)))
 
 
 def moe_lora_fused_shrink_expand_ex(x, lora_a, lora_b, y, sorted_token_ids, expert_ids, num_tokens_post_padded,

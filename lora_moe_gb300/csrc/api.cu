@@ -277,6 +277,38 @@ int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, 
   return resolve_path(f, path);
 }
 
+int moe_lora_fused_plan(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
+                        int block_size, int num_slices, int path, int sm_count, int max_smem_per_block,
+                        int32_t *out) {
+  if (!out || sm_count < 1 || max_smem_per_block < 1) return MOE_LORA_ERR_INVALID_ARG;
+  const int use = moe_lora_fused_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, block_size,
+                                              num_slices, path);
+  if (use < 0) return -use;
+  if (use == MOE_LORA_PATH_CUDA_CORE_STREAM) return MOE_LORA_ERR_UNSUPPORTED;
+  FusedArgs f = {};
+  f.M = M;
+  f.topk = topk;
+  f.num_experts = num_experts;
+  f.K = K;
+  f.N = N;
+  f.rank = rank;
+  f.max_loras = num_active_loras;
+  f.num_active_loras = num_active_loras;
+  f.block_size = block_size;
+  f.num_slices = num_slices;
+  DeviceInfo dev = {};
+  dev.sm_count = sm_count;
+  dev.major = 10;
+  dev.max_smem_optin = (size_t)max_smem_per_block;
+  FusedPlan plan = {};
+  const int st = use == MOE_LORA_PATH_TCGEN05 ? plan_fused_tcgen05(f, dev, &plan) : plan_fused_cuda_core(f, dev, &plan);
+  if (st) return st;
+  const int32_t vals[11] = {plan.kernel, plan.grid, plan.threads, plan.smem_bytes, plan.s_sh, plan.lag, plan.s_ex,
+                            plan.t_bufs, plan.tmem_cols, plan.cluster, plan.pairs_per_group};
+  for (int i = 0; i < 11; ++i) out[i] = vals[i];
+  return 0;
+}
+
 int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair, const moe_lora_bf16 *const *lora_a,
                                     const moe_lora_bf16 *const *lora_b, int num_slices, moe_lora_bf16 *y, int ldy,
                                     int y_offset, const float *topk_weights, const int32_t *sorted_token_ids,

@@ -629,6 +629,20 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   }
 }
 
+int plan_fused_cuda_core(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *out) {
+  if (f.block_size > kMaxBlock) return MOE_LORA_ERR_UNSUPPORTED;
+  CcCfg cfg;
+  if (int st = pick_cfg(f, dev, 8, &cfg)) return st;
+  out->kernel = MOE_LORA_PATH_CUDA_CORE_CLUSTER;
+  out->grid = 0;   // capped at run time by the clusters that can be resident at once
+  out->threads = kThreads;
+  out->smem_bytes = cfg.smem_bytes;
+  out->s_sh = out->lag = out->s_ex = out->t_bufs = out->tmem_cols = 0;
+  out->cluster = cfg.C;
+  out->pairs_per_group = cfg.pg;
+  return 0;
+}
+
 int launch_fused_naive(const FusedArgs &f, cudaStream_t stream) {
   DeviceInfo dev;
   if (int st = current_device_info(&dev)) return st;

@@ -362,9 +362,10 @@ int launch_bs(const FusedArgs &f, const stream::Cfg &cfg, const stream::TmapSet 
 
 bool tcgen05_path_supports(const FusedArgs &f) { return f.rank % 8 == 0 && f.num_active_loras <= stream::kMaxSlots; }
 
-int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream_) {
-  DeviceInfo dev;
-  if (int st = current_device_info(&dev)) return st;
+namespace {
+
+// Ring depths, TMEM columns, shared memory and grid of one call.
+int configure(const FusedArgs &f, const DeviceInfo &dev, stream::Cfg *out, long long *grid) {
   if (!tcgen05_path_supports(f)) return MOE_LORA_ERR_UNSUPPORTED;
   stream::Cfg cfg;
   // consumer region per T buffer: T_hi and T_lo tiles (bf16, swizzled)
@@ -384,14 +385,44 @@ int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream_) {
   // memory that they never need more than that.
   while (((228 * 1024) / (cfg.smem_bytes + 1024)) * cols > 512) cfg.smem_bytes += 4096;
   if (cfg.smem_bytes > (int)dev.max_smem_optin) return MOE_LORA_ERR_UNSUPPORTED;
-  stream::TmapSet maps;
-  if (int st = stream::make_tensor_maps(f, cfg, &maps)) return st;
   const long long bound = fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size);
-  if (bound <= 0) return 0;
   const int per_sm = std::max(1, (228 * 1024) / (cfg.smem_bytes + 1024));
   long long G = (long long)dev.sm_count * per_sm;
   if (G > bound * f.num_slices * cfg.nt_total) G = bound * f.num_slices * cfg.nt_total;
-  if (G < 1) G = 1;
+  *out = cfg;
+  *grid = bound <= 0 ? 0 : std::max(1LL, G);
+  return 0;
+}
+
+}  // namespace
+
+int plan_fused_tcgen05(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *out) {
+  stream::Cfg cfg;
+  long long G = 0;
+  if (int st = configure(f, dev, &cfg, &G)) return st;
+  out->kernel = MOE_LORA_PATH_TCGEN05;
+  out->grid = (int)G;
+  out->threads = kThreads;
+  out->smem_bytes = cfg.smem_bytes;
+  out->s_sh = cfg.s_sh;
+  out->lag = cfg.lag;
+  out->s_ex = cfg.s_ex;
+  out->t_bufs = cfg.t_bufs;
+  out->tmem_cols = cfg.tmem_cols;
+  out->cluster = 1;
+  out->pairs_per_group = f.block_size;
+  return 0;
+}
+
+int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream_) {
+  DeviceInfo dev;
+  if (int st = current_device_info(&dev)) return st;
+  stream::Cfg cfg;
+  long long G = 0;
+  if (int st = configure(f, dev, &cfg, &G)) return st;
+  if (G <= 0) return 0;
+  stream::TmapSet maps;
+  if (int st = stream::make_tensor_maps(f, cfg, &maps)) return st;
   switch (f.block_size) {
     case 16: return launch_bs<16>(f, cfg, maps, (int)G, stream_);
     case 32: return launch_bs<32>(f, cfg, maps, (int)G, stream_);

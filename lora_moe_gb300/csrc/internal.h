@@ -104,4 +104,14 @@ struct DeviceInfo {
 };
 int current_device_info(DeviceInfo *out);
 
+// The launch plan of a fused call (host arithmetic only).
+struct FusedPlan {
+  int kernel;                              // MOE_LORA_PATH_TCGEN05 or _CUDA_CORE_CLUSTER
+  int grid, threads, smem_bytes;
+  int s_sh, lag, s_ex, t_bufs, tmem_cols;  // tensor-core kernel: rings and TMEM
+  int cluster, pairs_per_group;            // cluster kernel: CTAs per block, pairs per group
+};
+int plan_fused_tcgen05(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *out);
+int plan_fused_cuda_core(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *out);
+
 }  // namespace moe_lora

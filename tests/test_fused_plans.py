@@ -1,0 +1,81 @@
+"""The launch plans of the fused kernels on a GB300 (152 SMs, 227 KB of
+opt-in shared memory per block), computed on the host: pinned for the
+benchmark workloads (a change to the shared-memory layout that costs ring
+depth shows up here, not only in a benchmark), and checked for invariants
+over a sweep of shapes."""
+import itertools
+
+import pytest
+
+from lora_moe_gb300 import binding as B
+from lora_moe_gb300 import inputs as gen
+
+GB300 = dict(sm_count=152, max_smem_per_block=232448)
+
+
+def plan_of(w, **kw):
+    return B.fused_plan(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size, **kw, **GB300)
+
+
+# (kernel, shrink stages, lag, expand stages, T buffers, TMEM columns) for the
+# tensor-core kernel; (kernel, CTAs per cluster, pairs per group) for the
+# cluster kernel.  These are the plans the measured numbers were taken with.
+PINNED = {
+    "decode_gptoss_w2": (B.PATH_TCGEN05, 10, 4, 6, 1, 128),
+    "prefill_mixtral_w13": (B.PATH_TCGEN05, 10, 4, 6, 1, 256),
+    "large_e_nact1": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
+    "large_e_nact8": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
+    "decode_qwen3_w13": (B.PATH_CUDA_CORE_CLUSTER, 8, 8),
+    "tiny": (B.PATH_CUDA_CORE_CLUSTER, 1, 8),
+}
+
+
+@pytest.mark.parametrize("name", sorted(PINNED))
+def test_benchmark_plans_pinned(name):
+    p = plan_of(gen.WORKLOADS[name])
+    want = PINNED[name]
+    if want[0] == B.PATH_TCGEN05:
+        got = (p["kernel"], p["s_sh"], p["lag"], p["s_ex"], p["t_bufs"], p["tmem_cols"])
+    else:
+        got = (p["kernel"], p["cluster"], p["pairs_per_group"])
+    assert got == want, p
+
+
+SHAPES = list(itertools.product([16, 256, 4096], [2, 8], [8, 128, 256], [1024, 4096, 7168], [1536, 4096, 28672],
+                                [8, 16, 64, 128], [16, 64, 128]))
+
+
+@pytest.mark.parametrize("path", [B.PATH_TCGEN05, B.PATH_CUDA_CORE_CLUSTER])
+def test_plan_invariants(path):
+    checked = 0
+    for M, topk, E, K, N, r, bs in SHAPES:
+        if topk > E:
+            continue
+        try:
+            p = B.fused_plan(M, topk, E, K, N, r, 2, bs, path=path, **GB300)
+        except B.MoeLoraError:
+            continue
+        checked += 1
+        assert p["kernel"] == path
+        assert 0 < p["smem_bytes"] <= GB300["max_smem_per_block"]
+        if path == B.PATH_TCGEN05:
+            # a next B tile loads under the MMA -- except at block size 128 with
+            # rank > 64, where two expand stages (64 KB each) do not fit beside the
+            # 32 KB shrink stages and the 64 KB T buffer
+            if not (bs == 128 and r > 64):
+                assert p["s_ex"] >= 2, (M, topk, E, K, N, r, bs, p)
+            assert p["s_sh"] >= 2 * p["lag"] + 1, p                       # the shrink producers cannot deadlock
+            assert p["tmem_cols"] in (32, 64, 128, 256, 512)
+            per_sm = max(1, (228 * 1024) // (p["smem_bytes"] + 1024))
+            assert per_sm * p["tmem_cols"] <= 512, p                      # co-resident CTAs fit in TMEM
+            assert p["threads"] == 416 and 1 <= p["grid"] <= 152 * per_sm
+        else:
+            assert 1 <= p["cluster"] <= 16 and p["pairs_per_group"] in (1, 2, 8)
+    assert checked > 100
+
+
+def test_plan_rejects_what_the_kernel_cannot_run():
+    with pytest.raises(B.MoeLoraError):
+        B.fused_plan(64, 4, 128, 2880, 2880, 12, 6, 16, path=B.PATH_TCGEN05, **GB300)   # rank % 8 != 0
+    with pytest.raises(B.MoeLoraError):
+        B.fused_plan(64, 4, 128, 2880, 2880, 64, 6, 16, path=B.PATH_CUDA_CORE_STREAM, **GB300)
