@@ -189,3 +189,40 @@ def test_fused_naive_argument_errors():
     assert naive(nact=0) == 0          # zero grid
     assert naive(M=0) == 0
     assert naive() == 1                # NULL buffers
+
+
+def test_plain_c_consumer(tmp_path):
+    """The header compiles as C11 under -Wall -Wextra -pedantic, and a C
+    program links against the library and calls its host-only functions."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    lib_dir = os.path.dirname(B.library_path())
+    src = tmp_path / "consumer.c"
+    src.write_text(r"""
+#include <stdio.h>
+#include <string.h>
+#include "moe_lora.h"
+int main(void) {
+  int32_t plan[11];
+  if (moe_lora_version() <= 0) return 1;
+  if (moe_lora_max_num_tokens_padded(16, 8, 128, 16) != 16 * 8 + 128 * 15) return 2;
+  if (moe_lora_max_num_m_blocks(16, 8, 128, 16) != (16 * 8 + 128 * 15 + 15) / 16) return 3;
+  if (strlen(moe_lora_status_string(MOE_LORA_ERR_INVALID_ARG)) == 0) return 4;
+  if (moe_lora_fused_resolve_path(16, 8, 128, 2048, 1536, 16, 2, 16, 1, MOE_LORA_PATH_AUTO)
+      != MOE_LORA_PATH_CUDA_CORE_CLUSTER) return 5;
+  if (moe_lora_fused_plan(8192, 2, 8, 4096, 28672, 16, 4, 64, 1, MOE_LORA_PATH_AUTO, 152, 232448, plan) != 0)
+    return 6;
+  if (plan[0] != MOE_LORA_PATH_TCGEN05) return 7;
+  printf("ok\n");
+  return 0;
+}
+""")
+    exe = tmp_path / "consumer"
+    subprocess.check_call(["gcc", "-std=c11", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                           "-I", os.path.join(root, "include"), str(src), "-L", lib_dir, "-lmoe_lora",
+                           "-Wl,-rpath," + lib_dir, "-o", str(exe)])
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0 and out.stdout.strip() == "ok", (out.returncode, out.stdout, out.stderr)
