@@ -153,17 +153,9 @@ __device__ bool write_segments(const AlignArgs &a, int l, const int *cnt, int *o
   const int sentinel = a.M * a.topk;
   if (tid < E)
     for (int i = excl + c; i < excl + padded; ++i) sorted[i] = sentinel;
-  const int nblocks = total / bs;
-  for (int b = tid; b < nblocks; b += blockDim.x) {
-    // the expert whose segment [off[e], off[e+1]) holds position b*bs
-    const int pos = b * bs;
-    int lo = 0, hi = E;   // invariant: off[lo] <= pos < off[hi]
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (off[mid] <= pos) lo = mid; else hi = mid;
-    }
-    experts[b] = lo;
-  }
+  // each expert's thread labels the blocks of its own segment
+  if (tid < E)
+    for (int b = excl / bs; b < (excl + padded) / bs; ++b) experts[b] = tid;
   return true;
 }
 

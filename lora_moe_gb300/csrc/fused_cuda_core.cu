@@ -363,6 +363,9 @@ __global__ void __launch_bounds__(kThreads, 4) fused_cuda_core_kernel(const Fuse
     if (tid < bs && b_first * bs + tid < p.max_num_tokens_padded)
       f_first = __ldg(p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + b_first * bs + tid);
     nitems = min(__ldg(p.num_tokens_post_padded + l) / bs, p.max_num_m_blocks);
+    // the first block's ids were requested with the count: keep them there
+    // (not sunk below the exit test), so that one round trip brings all three
+    asm volatile("" ::"r"(e_first), "r"(f_first));
     if (b_first >= nitems) return;
   } else if (c == 0 && tid == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
     for (int i = 0; i < p.num_active_loras; ++i) {
