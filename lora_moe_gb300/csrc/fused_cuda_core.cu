@@ -16,16 +16,23 @@
 // megabytes per call, by latency.  Design:
 //   * grid (C, num_slices * num_active_loras, blocks): CTA (c, s * nact + z, b)
 //     serves slice s of block b of slot z (vLLM PR #32005: the LoRA grid
-//     dimension is the number of active LoRAs); blocks past
-//     num_tokens_post_padded exit after one dependent load.
+//     dimension is the number of active LoRAs), capped at the clusters that
+//     can be resident at once (CTAs then walk further blocks); blocks past
+//     num_tokens_post_padded exit after one dependent load.  With naive block
+//     assignment the grid is (C, num_slices, pairs) and each work item is one
+//     pair, its LoRA and expert read from token_lora_mapping and topk_ids.
 //   * a thread-block cluster of C CTAs shares a block: CTA c streams the
 //     K-slice c of A and of the gathered x rows and the N-slice c of B and y;
 //     the C partial t's are summed through distributed shared memory in rank
 //     order (deterministic).
-//   * every operand is requested at once, before the first wait: A, x and y_in
-//     rows with 16-byte cp.async (load/store unit), the contiguous B slice with
-//     one bulk copy.  Dot products read 16-byte shared-memory vectors and reduce
+//   * operands are requested before the first wait: the A slice (16-byte
+//     cp.async) and the contiguous B slice (one bulk copy) as soon as the
+//     expert id is known, the x and y_in rows once the block's pairs are
+//     compacted.  Dot products read 16-byte shared-memory vectors and reduce
 //     with warp shuffles; y is written with coalesced stores.
+//   * pairs are processed in groups whose size is a template constant (2 for
+//     blocks with at most two real pairs, else 8), so no shuffle sits in
+//     divergent code.
 #include <cooperative_groups.h>
 #include <algorithm>
 #include <mutex>
