@@ -249,9 +249,7 @@ def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: in
     Returns (us_per_step, description, calls_made)."""
     import oracle
     w = inp.w
-    act = set(int(v) for v in inp.lora_ids)
-    cov = np.array([int(inp.token_lora_mapping[f // w.topk]) in act for f in range(w.M * w.topk)])
-    cov_idx = np.flatnonzero(cov).astype(np.int32)
+    cov_idx = _covered_pairs(inp)
     cols = np.arange(w.N, dtype=np.int32)
     n = max(1, min(pairs_per_call, len(cov_idx)))
     t_align = t_fused = 0.0
@@ -264,13 +262,8 @@ def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: in
             oracle.align(inp.topk_ids, inp.token_lora_mapping, inp.lora_ids, w.E, w.max_loras, w.block_size)
         t1 = time.perf_counter()
         sel = cov_idx[(made * n + np.arange(n)) % max(1, len(cov_idx))] if len(cov_idx) else cov_idx
-        if len(sel) and ex is not None:
-            oracle.fused_ex(ex.x, ex.lora_a, ex.lora_b, ex.y_in, inp.topk_ids, inp.token_lora_mapping,
-                            inp.lora_ids, topk_weights=ex.topk_weights, x_per_pair=ex.x_per_pair,
-                            y_offset=ex.y_offset, pairs=sel)
-        elif len(sel):
-            oracle.fused_sampled(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
-                                 inp.lora_ids, sel, cols)
+        if len(sel):
+            _oracle_pairs(inp, ex, sel, cols)
         t2 = time.perf_counter()
         t_align += t1 - t0
         t_fused += t2 - t1
@@ -286,6 +279,84 @@ def time_oracle(inp: gen.Inputs, budget_s: float, pairs_per_call: int, calls: in
     desc = ("%soracle fused over %d of %d covered pairs per call (all %d columns), %d calls, scaled to one "
             "full step" % ("oracle align over the whole batch + " if with_align else "", n, len(cov_idx), w.N, made))
     return us, desc, made
+
+
+def _covered_pairs(inp: gen.Inputs):
+    w = inp.w
+    act = set(int(v) for v in inp.lora_ids)
+    cov = np.array([int(inp.token_lora_mapping[f // w.topk]) in act for f in range(w.M * w.topk)])
+    return np.flatnonzero(cov).astype(np.int32)
+
+
+def _oracle_pairs(inp: gen.Inputs, ex, sel, cols):
+    """One oracle call of the fused stage at the flat pairs `sel` (every column)."""
+    import oracle
+    if ex is not None:
+        return oracle.fused_ex(ex.x, ex.lora_a, ex.lora_b, ex.y_in, inp.topk_ids, inp.token_lora_mapping,
+                               inp.lora_ids, topk_weights=ex.topk_weights, x_per_pair=ex.x_per_pair,
+                               y_offset=ex.y_offset, pairs=sel)
+    return oracle.fused_sampled(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
+                                inp.lora_ids, sel, cols)
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def time_oracle_threads(inp: gen.Inputs, budget_s: float, pairs_per_thread: int, threads: int, ex=None,
+                        with_align=True):
+    """The same oracle, its fused stage spread over `threads` host threads.
+
+    Every call's pairs are cut into `threads` contiguous chunks, one oracle
+    call per chunk on its own thread; the oracle is a C library entered through
+    ctypes, which drops the GIL for the call, and each pair's output depends on
+    that pair alone, so the chunks run in parallel and need no merging beyond
+    concatenation.  The align (one sequential pass over the batch) stays on the
+    calling thread.  The first call's output is checked equal, element for
+    element, to one single-threaded oracle call on the same pairs.
+
+    Returns (us_per_step, description, threads)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    w = inp.w
+    cov_idx = _covered_pairs(inp)
+    cols = np.arange(w.N, dtype=np.int32)
+    threads = max(1, min(threads, len(cov_idx))) if len(cov_idx) else 1
+    n = max(1, min(pairs_per_thread * threads, len(cov_idx)))
+    t_align = t_fused = 0.0
+    done_pairs = made = 0
+    with ThreadPoolExecutor(max_workers=threads) as pool:
+        t_start = time.perf_counter()
+        while True:
+            t0 = time.perf_counter()
+            if with_align:
+                oracle.align(inp.topk_ids, inp.token_lora_mapping, inp.lora_ids, w.E, w.max_loras, w.block_size)
+            t1 = time.perf_counter()
+            sel = cov_idx[(made * n + np.arange(n)) % max(1, len(cov_idx))] if len(cov_idx) else cov_idx
+            if len(sel):
+                chunks = [c for c in np.array_split(sel, threads) if len(c)]
+                outs = list(pool.map(lambda c: _oracle_pairs(inp, ex, c, cols), chunks))
+            t2 = time.perf_counter()
+            if made == 0 and len(sel):
+                one = _oracle_pairs(inp, ex, sel, cols)
+                if not np.array_equal(np.concatenate(outs, axis=0), one, equal_nan=True):
+                    raise RuntimeError("threaded oracle run differs from the single-threaded one")
+            t_align += t1 - t0
+            t_fused += t2 - t1
+            done_pairs += len(sel)
+            made += 1
+            if time.perf_counter() - t_start >= budget_s:
+                break
+    per_pair = t_fused / max(1, done_pairs)
+    us = (t_align / made + per_pair * len(cov_idx)) * 1e6
+    desc = ("%soracle fused over %d of %d covered pairs per call split over %d threads (all %d columns), "
+            "%d calls, scaled to one full step; first call checked equal to a single-threaded run"
+            % ("single-threaded oracle align over the whole batch + " if with_align else "", n, len(cov_idx),
+               threads, w.N, made))
+    return us, desc, threads
 
 
 # --------------------------------------------------------------------------- GPU side
@@ -584,10 +655,13 @@ def main():
         return
     counts = res["counts"]
     us_per_step = res["ms"] * 1e3 / (args.steps * world)
-    cpu = None
+    cpu = cpu_threads = None
     if rank == 0 and not args.no_cpu_baseline:
         us, desc, made = time_oracle(res["inp"], 12.0, 8, ex=res["ex"], with_align=not args.naive)
         cpu = {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": desc}
+        us_t, desc_t, nt = time_oracle_threads(res["inp"], 4.0, 8, host_threads(), ex=res["ex"],
+                                               with_align=not args.naive)
+        cpu_threads = {"value": us_t, "unit": "us/call", "cores": nt, "kind": "oracle", "sample": desc_t}
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()
@@ -617,6 +691,7 @@ def main():
                      "traffic": None if uses_ex(args) else NCU_TRAFFIC.get((w.name, res["kernel_name"])),
                      "traffic_unit": "bytes per launch (ncu)"},
         "cpu_baseline": cpu,
+        "cpu_baseline_threads": cpu_threads,
         "e2e": res["e2e"],
         "gpu_launches": args.steps * (res["align_launches"] + 1),
         "clocks": res["clocks"],
