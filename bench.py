@@ -20,7 +20,8 @@ Options of the general fused call (moe_lora_fused_shrink_expand_ex), off by
 default: --slices S (separate adapters per slice, e.g. 2 for w13's gate and
 up), --per-pair-x (one input row per pair, the w2 stage), --routed-weight
 (delta scaled by the router weight).  With any of them the step runs the
-general call instead of the plain one.
+general call instead of the plain one.  --align-variant 1|2 forces the
+shared-memory or the global-memory align (default: the library's choice).
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores
 instead, on a bounded sample of pairs per step, scaled to microseconds per
@@ -60,6 +61,8 @@ def parse():
     ap.add_argument("--profile-steps", type=int, default=0,
                     help="only run W + this many eager steps (for ncu); prints no JSON line")
     ap.add_argument("--path", type=int, default=0, help="fused path: 0 auto, 1 CUDA cores, 2 tcgen05, 3 CUDA-core cluster, 4 CUDA-core streaming")
+    ap.add_argument("--align-variant", type=int, default=0, choices=[0, 1, 2],
+                    help="align variant: 0 auto, 1 shared memory (one CTA per slot), 2 global memory (three launches)")
     ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0: enough to exceed 3x L2)")
     ap.add_argument("--slices", type=int, default=1, help="adapter slices per layer (general call)")
     ap.add_argument("--per-pair-x", action="store_true", help="one input row per pair (general call)")
@@ -396,7 +399,8 @@ def run_ours(args, world, rank, local, pg):
     sets = []
     for i in range(NB):
         s = {k: v.clone() for k, v in base.items()}
-        s["buf"] = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size, device=dev)
+        s["buf"] = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size, device=dev,
+                                  variant=args.align_variant)
         sets.append(s)
     del base
     err = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -408,7 +412,7 @@ def run_ours(args, world, rank, local, pg):
         b = s["buf"]
         B.moe_lora_align(s["topk_ids"], s["mapping"], s["lora_ids"], w.E, w.max_loras, w.block_size,
                          b.sorted_token_ids, b.expert_ids, b.num_tokens_post_padded, workspace=b.workspace,
-                         err_flag=err, stream=stream)
+                         variant=args.align_variant, err_flag=err, stream=stream)
 
     def fused(s):
         b = s["buf"]
@@ -537,7 +541,8 @@ def run_ours(args, world, rank, local, pg):
                 v[name] = dev_pack[off:off + arr.nbytes].view(tdt[name]).view(arr.shape)
             for name in base_keys_adapters:
                 v[name] = sets[0][name]
-            v["buf"] = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size, device=dev)
+            v["buf"] = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size,
+                                      device=dev, variant=args.align_variant)
             packs.append(v)
         out_host = torch.empty(src.y_in.shape, dtype=torch.int16).pin_memory()
         h2d = total
@@ -605,12 +610,16 @@ def run_ours(args, world, rank, local, pg):
 
 
 def ex_config(args):
-    """Config keys of the general call's options (none for the plain call)."""
-    if not uses_ex(args):
-        return {}
-    d = {"num_slices": args.slices, "x_per_pair": bool(args.per_pair_x), "routed_weight": bool(args.routed_weight)}
-    if args.naive:
-        d["block_assignment"] = "naive (no align)"
+    """Config keys of the options off the default: the general call's (none
+    for the plain call) and a forced align variant."""
+    d = {}
+    if uses_ex(args):
+        d = {"num_slices": args.slices, "x_per_pair": bool(args.per_pair_x),
+             "routed_weight": bool(args.routed_weight)}
+        if args.naive:
+            d["block_assignment"] = "naive (no align)"
+    if args.align_variant:
+        d["align_variant"] = {1: "smem (forced)", 2: "global (forced)"}[args.align_variant]
     return d
 
 

@@ -109,3 +109,11 @@ def test_json_line_carries_the_contract_keys(monkeypatch, capsys, tiny):
     assert d["cpu_baseline"] == {"value": 5.0, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": "s1"}
     assert d["cpu_baseline_threads"]["cores"] == 4 and d["cpu_baseline_threads"]["value"] == 2.0
     assert d["gpu_launches"] == 4 * 2
+
+
+@pytest.mark.parametrize("v,name", [(0, None), (1, "smem (forced)"), (2, "global (forced)")])
+def test_forced_align_variant_is_named_in_the_config(monkeypatch, v, name):
+    import sys
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--align-variant", str(v)])
+    cfg = bench.ex_config(bench.parse())
+    assert cfg.get("align_variant") == name
