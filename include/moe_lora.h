@@ -64,7 +64,7 @@ typedef enum {
     MOE_LORA_ERR_MISALIGNED = 3,    /* a pointer or a row is not 16-byte aligned */
     MOE_LORA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required */
     MOE_LORA_ERR_LAUNCH = 5,        /* a CUDA launch or attribute call failed */
-    MOE_LORA_ERR_DEVICE = 6         /* no usable sm_100-family device is current */
+    MOE_LORA_ERR_DEVICE = 6         /* the current device is not compute capability 10.3 (sm_103) */
 } moe_lora_status;
 
 /* Bits OR-ed into *err_flag by the kernels. */

@@ -29,8 +29,9 @@ int current_device_info(DeviceInfo *out) {
     have[dev] = true;
   }
   *out = cache[dev];
-  // The kernels are built for sm_103a (tcgen05, TMA, clusters).
-  if (out->major != 10) return MOE_LORA_ERR_DEVICE;
+  // The kernels are built for sm_103a only (tcgen05, TMA, clusters); an
+  // arch-specific image loads on compute capability 10.3 alone.
+  if (out->major != 10 || out->minor != 3) return MOE_LORA_ERR_DEVICE;
   return 0;
 }
 
@@ -299,6 +300,7 @@ int moe_lora_fused_plan(int M, int topk, int num_experts, int K, int N, int rank
   DeviceInfo dev = {};
   dev.sm_count = sm_count;
   dev.major = 10;
+  dev.minor = 3;
   dev.max_smem_optin = (size_t)max_smem_per_block;
   FusedPlan plan = {};
   const int st = use == MOE_LORA_PATH_TCGEN05 ? plan_fused_tcgen05(f, dev, &plan) : plan_fused_cuda_core(f, dev, &plan);
