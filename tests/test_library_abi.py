@@ -12,15 +12,28 @@ from lora_moe_gb300 import binding as B
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "moe_lora.h")
 
 
-def declared_functions():
+def _header_code():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(moe_lora_[a-z0-9_]+)\s*\(", text)))
+    return "\n".join(l for l in text.splitlines() if not l.lstrip().startswith("#"))
+
+
+def declared_functions():
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", _header_code())))
 
 
 def test_header_declares_the_two_stages():
     names = declared_functions()
     assert "moe_lora_align" in names and "moe_lora_fused_shrink_expand" in names
+    assert "moe_align_block_size" in names
+
+
+def test_every_header_declaration_is_parsed():
+    """One name per function declaration: a declaration whose name the parser
+    missed would escape the export check below."""
+    code = _header_code().replace('extern "C" {', "").replace("}", "};")
+    decls = [d for d in code.split(";") if "(" in d]
+    assert len(decls) == len(declared_functions()), decls
 
 
 def test_library_exports_every_declared_symbol():
