@@ -229,6 +229,25 @@ int main(void) {
   if (moe_lora_fused_plan(8192, 2, 8, 4096, 28672, 16, 4, 64, 1, MOE_LORA_PATH_AUTO, 152, 232448, plan) != 0)
     return 6;
   if (plan[0] != MOE_LORA_PATH_TCGEN05) return 7;
+  /* every device entry point links from C; argument errors return before any CUDA call */
+  {
+    const moe_lora_bf16 *a[1] = {NULL}, *b[1] = {NULL};
+    if (moe_lora_align(NULL, NULL, NULL, NULL, 16, 0, 8, 2, 2, 16, NULL, NULL, NULL, 152, 10, NULL, 0,
+                       MOE_LORA_ALIGN_AUTO, NULL, NULL) != MOE_LORA_ERR_INVALID_ARG) return 8;
+    if (moe_align_block_size(NULL, 16, 2, 8, 8, NULL, NULL, NULL, 152, 10, NULL, 0, MOE_LORA_ALIGN_AUTO, NULL,
+                             NULL) != MOE_LORA_ERR_UNSUPPORTED) return 9;
+    if (moe_lora_align_static_workspace(NULL, NULL, NULL, NULL, 16, 0, 8, 2, 0, 16, NULL, NULL, NULL, 152, 10,
+                                        NULL, NULL) != MOE_LORA_ERR_INVALID_ARG) return 10;
+    if (moe_lora_fused_shrink_expand(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 16, 2, 8, 256, 512, 132,
+                                     2, 2, 16, 152, 10, 1, MOE_LORA_PATH_AUTO, NULL, NULL)
+        != MOE_LORA_ERR_UNSUPPORTED) return 11;
+    if (moe_lora_fused_shrink_expand_ex(NULL, 0, a, b, 0, NULL, 512, 0, NULL, NULL, NULL, NULL, NULL, NULL, 16, 2,
+                                        8, 256, 512, 8, 2, 2, 16, 152, 10, 1, MOE_LORA_PATH_AUTO, NULL, NULL)
+        != MOE_LORA_ERR_INVALID_ARG) return 12;
+    if (moe_lora_fused_shrink_expand_naive(NULL, 0, a, b, 1, NULL, 512, 0, NULL, NULL, NULL, NULL, NULL, 16, 2, 8,
+                                           260, 512, 8, 2, 2, 1, NULL, NULL) != MOE_LORA_ERR_MISALIGNED) return 13;
+    if (moe_lora_align_workspace_bytes(4096, 8, 256, 1, 64, MOE_LORA_ALIGN_GLOBAL) == 0) return 14;
+  }
   printf("ok\n");
   return 0;
 }
