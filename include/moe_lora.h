@@ -198,9 +198,12 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, int num_exper
  * aligned; other limits as for moe_lora_align.  path: MOE_LORA_PATH_*; AUTO
  * picks the tensor-core path (when rank % 8 == 0) for batches of at least
  * 1024 pairs or when the adapters the call may touch (block bound times
- * (K + N) * rank * 2 bytes) exceed 48 MB, and the cluster kernel otherwise;
- * MOE_LORA_PATH_CUDA_CORE runs the cluster kernel
- * (MOE_LORA_PATH_CUDA_CORE_CLUSTER).
+ * (K + N) * rank * 2 bytes) exceed 48 MB, and the cluster kernel otherwise --
+ * unless the cluster kernel cannot hold a CTA's share of the adapter rows in
+ * shared memory (long N * rank or K * rank rows), in which case it also picks
+ * the tensor-core path when K >= 64 and N >= 32.  Shapes neither kernel
+ * takes return MOE_LORA_ERR_UNSUPPORTED.  MOE_LORA_PATH_CUDA_CORE runs the
+ * cluster kernel (MOE_LORA_PATH_CUDA_CORE_CLUSTER).
  */
 int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a,
                                  const moe_lora_bf16 *lora_b, moe_lora_bf16 *y,
@@ -274,7 +277,8 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair,
  * [0, max_loras) as MOE_LORA_DEVERR_LORA_ID.  Pairs that share an adapter
  * each read it (from L2 after the first), so this path suits batches with
  * few pairs per (LoRA, expert), i.e. decode.  Runs on CUDA cores (the
- * cluster kernel).
+ * cluster kernel); shapes whose adapter rows that kernel cannot hold in
+ * shared memory return MOE_LORA_ERR_UNSUPPORTED.
  *
  *   topk_ids          [device] int32 [M, topk]
  *   token_lora_mapping [device] int32 [M] (-1: no adapter)
@@ -296,7 +300,8 @@ int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair,
  * runs: MOE_LORA_PATH_TCGEN05, MOE_LORA_PATH_CUDA_CORE_CLUSTER or
  * MOE_LORA_PATH_CUDA_CORE_STREAM (never AUTO or CUDA_CORE), or a negative
  * moe_lora_status code if `path` is not valid for these sizes.  Host only; no
- * device is touched.
+ * device is touched: where AUTO depends on shared memory it assumes the
+ * 227 KB per block of compute capability 10.3.
  */
 int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank,
                                 int num_active_loras, int block_size, int num_slices, int path);

@@ -175,20 +175,43 @@ static int prepare_fused(const moe_lora_bf16 *x, int x_per_pair, const moe_lora_
   return 0;
 }
 
+// Opt-in shared memory per block on compute capability 10.3 (227 KB): what the
+// host-only queries plan against when no device is asked.
+constexpr int kSmemOptinSm103 = 232448;
+
+// Whether the cluster kernel can hold a CTA's slices of A and B (and its x
+// and y rows) in shared memory with at most 16 CTAs per block.  Host
+// arithmetic only.
+static bool cluster_kernel_fits(const FusedArgs &f, size_t max_smem) {
+  DeviceInfo dev = {};
+  dev.major = 10;
+  dev.minor = 3;
+  dev.max_smem_optin = max_smem;
+  FusedPlan plan = {};
+  return plan_fused_cuda_core(f, dev, &plan) == 0;
+}
+
 // The kernel a fused call runs.  AUTO takes the tensor-core kernel (when it
 // supports the sizes) for batches of at least 1024 pairs or when the adapter
 // bytes the call may touch, by the block bound, exceed 48 MB: there the
 // balanced persistent tile ranges keep every SM streaming.  Otherwise, and for
 // MOE_LORA_PATH_CUDA_CORE, the cluster kernel: on every decode workload
 // measured it beat the streaming CUDA-core kernel, which recomputes the shrink
-// of a block in every CTA whose tile range touches it.
-static int resolve_path(const FusedArgs &f, int path) {
+// of a block in every CTA whose tile range touches it.  Small batches whose
+// adapter rows are too long for the cluster kernel's shared memory (N * rank
+// or K * rank beyond what 16 CTAs hold) also go to the tensor-core kernel when
+// K and N span at least one 64-wide K tile and 32 output columns.
+static int resolve_path(const FusedArgs &f, int path, size_t max_smem) {
   int use = path;
   if (use == MOE_LORA_PATH_AUTO) {
     const double touched = (double)fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size) *
                            f.num_slices * (double)(f.K + f.N) * f.rank * 2.0;
     const bool big = (long long)f.M * f.topk >= 1024 || touched > 48.0e6;
-    use = (big && tcgen05_path_supports(f)) ? MOE_LORA_PATH_TCGEN05 : MOE_LORA_PATH_CUDA_CORE;
+    const bool tc = tcgen05_path_supports(f);
+    if (tc && (big || (f.K >= 64 && f.N >= 32 && !cluster_kernel_fits(f, max_smem))))
+      use = MOE_LORA_PATH_TCGEN05;
+    else
+      use = MOE_LORA_PATH_CUDA_CORE;
   }
   if (use == MOE_LORA_PATH_CUDA_CORE) use = MOE_LORA_PATH_CUDA_CORE_CLUSTER;
   return use;
@@ -206,7 +229,7 @@ const char *moe_lora_status_string(int status) {
     case MOE_LORA_ERR_MISALIGNED: return "pointer or row not 16-byte aligned";
     case MOE_LORA_ERR_WORKSPACE: return "workspace missing or too small";
     case MOE_LORA_ERR_LAUNCH: return "CUDA launch failed";
-    case MOE_LORA_ERR_DEVICE: return "no usable sm_100-family device";
+    case MOE_LORA_ERR_DEVICE: return "no usable device (compute capability 10.3 required)";
     default: return "unknown status";
   }
 }
@@ -257,8 +280,8 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, int num_exper
                     workspace_bytes, variant, err_flag, stream);
 }
 
-int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
-                                int block_size, int num_slices, int path) {
+static int resolve_path_query(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
+                              int block_size, int num_slices, int path, size_t max_smem) {
   if (M < 0 || topk < 1 || num_experts < 1 || K < 8 || N < 8 || rank < 1 || num_active_loras < 0 ||
       num_slices < 1 || num_slices > kMaxSlices || path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_CUDA_CORE_STREAM)
     return -MOE_LORA_ERR_INVALID_ARG;
@@ -275,15 +298,21 @@ int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, 
   f.num_active_loras = num_active_loras;
   f.block_size = block_size;
   f.num_slices = num_slices;
-  return resolve_path(f, path);
+  return resolve_path(f, path, max_smem);
+}
+
+int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
+                                int block_size, int num_slices, int path) {
+  return resolve_path_query(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices, path,
+                            kSmemOptinSm103);
 }
 
 int moe_lora_fused_plan(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
                         int block_size, int num_slices, int path, int sm_count, int max_smem_per_block,
                         int32_t *out) {
   if (!out || sm_count < 1 || max_smem_per_block < 1) return MOE_LORA_ERR_INVALID_ARG;
-  const int use = moe_lora_fused_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, block_size,
-                                              num_slices, path);
+  const int use = resolve_path_query(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices,
+                                     path, (size_t)max_smem_per_block);
   if (use < 0) return -use;
   if (use == MOE_LORA_PATH_CUDA_CORE_STREAM) return MOE_LORA_ERR_UNSUPPORTED;
   FusedArgs f = {};
@@ -339,7 +368,9 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair, cons
   f.block_size = block_size;
   f.max_num_tokens_padded = max_num_tokens_padded;
   f.max_num_m_blocks = max_num_m_blocks;
-  const int use = resolve_path(f, path);
+  DeviceInfo dev;
+  if (int st = current_device_info(&dev)) return st;
+  const int use = resolve_path(f, path, dev.max_smem_optin);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (use) {
     case MOE_LORA_PATH_TCGEN05: return launch_fused_tcgen05(f, s);

@@ -74,6 +74,55 @@ def test_plan_invariants(path):
     assert checked > 100
 
 
+def test_cluster_never_leaves_a_cta_without_columns():
+    """Every CTA of a cluster holds at least one 8-element chunk of K and of N
+    (so each adapter copy is at least 16 bytes), down to the smallest rows."""
+    checked = rejected = 0
+    for K, N, r in itertools.product([8, 16, 24, 40, 64, 136, 1024], [8, 16, 24, 40, 64, 136, 1024],
+                                     [4, 8, 12, 16, 64, 128]):
+        try:
+            p = B.fused_plan(16, 2, 8, K, N, r, 2, 16, path=B.PATH_CUDA_CORE_CLUSTER, **GB300)
+        except B.MoeLoraError:
+            # only when even the largest cluster leaves a CTA more A and B rows
+            # than shared memory holds
+            C = min(16, K // 8, N // 8)
+            kslice, nslice = -(-(K // 8) // C) * 8, -(-(N // 8) // C) * 8
+            assert r * (kslice + 8) * 2 + nslice * r * 2 > GB300["max_smem_per_block"], (K, N, r)
+            rejected += 1
+            continue
+        assert 1 <= p["cluster"] <= min(16, K // 8, N // 8), (K, N, r, p)
+        checked += 1
+    assert checked + rejected == 7 * 7 * 6 and rejected <= 2
+
+
+def test_auto_sends_rows_too_long_for_the_cluster_kernel_to_tensor_cores():
+    """One-token decode with w13-sized rows: N * rank beyond what 16 cluster
+    CTAs hold in shared memory goes to the tensor-core kernel; short rows stay
+    on the cluster kernel."""
+    R = B.fused_resolve_path
+    assert R(1, 1, 8, 4096, 28672, 64, 1, 16) == B.PATH_TCGEN05
+    assert R(1, 2, 8, 4096, 14336, 128, 1, 16) == B.PATH_TCGEN05
+    assert R(1, 1, 8, 4096, 1536, 64, 1, 16) == B.PATH_CUDA_CORE_CLUSTER
+    with pytest.raises(B.MoeLoraError):   # the cluster kernel itself cannot hold these rows
+        B.fused_plan(1, 1, 8, 4096, 28672, 64, 1, 16, path=B.PATH_CUDA_CORE_CLUSTER, **GB300)
+    assert B.fused_plan(1, 1, 8, 4096, 28672, 64, 1, 16, **GB300)["kernel"] == B.PATH_TCGEN05
+
+
+def test_auto_plans_every_shape_with_a_full_k_tile():
+    """AUTO finds a kernel for every supported shape with K >= 64, N >= 32
+    and rank % 8 == 0, from one-token decode to prefill batches."""
+    n = 0
+    for M, topk, E, K, N, r, bs, nact in itertools.product(
+            [1, 16, 200, 4096], [1, 8], [8, 256], [64, 1024, 7168], [32, 1536, 14336, 28672], [8, 64, 128],
+            [16, 128], [1, 4]):
+        if topk > E:
+            continue
+        p = B.fused_plan(M, topk, E, K, N, r, nact, bs, **GB300)
+        assert p["kernel"] in (B.PATH_TCGEN05, B.PATH_CUDA_CORE_CLUSTER)
+        n += 1
+    assert n > 1000
+
+
 def test_plan_rejects_what_the_kernel_cannot_run():
     with pytest.raises(B.MoeLoraError):
         B.fused_plan(64, 4, 128, 2880, 2880, 12, 6, 16, path=B.PATH_TCGEN05, **GB300)   # rank % 8 != 0
