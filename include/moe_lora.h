@@ -195,10 +195,12 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, int num_exper
  *   adapter_enabled  [device] int32 [max_loras] or NULL
  * Sizes: 1 <= rank <= 128 with rank % 4 == 0 (the tensor-core path needs
  * rank % 8 == 0); K % 8 == 0 and N % 8 == 0; x, lora_a, lora_b, y 16-byte
- * aligned; other limits as for moe_lora_align.  path: MOE_LORA_PATH_*; AUTO
- * picks the tensor-core path (when rank % 8 == 0) for batches of at least
- * 1024 pairs or when the adapters the call may touch (block bound times
- * (K + N) * rank * 2 bytes) exceed 48 MB, and the cluster kernel otherwise --
+ * aligned; other limits as for moe_lora_align.  The tensor-core and
+ * streaming paths also need num_active_loras <= 128.
+ * path: MOE_LORA_PATH_*.  AUTO picks the tensor-core path (when it takes the
+ * sizes) for batches of at least 1024 pairs or when the adapters the call may
+ * touch (block bound times (K + N) * rank * 2 bytes) exceed 48 MB, and the
+ * cluster kernel otherwise --
  * unless the cluster kernel cannot hold a CTA's share of the adapter rows in
  * shared memory (long N * rank or K * rank rows), in which case it also picks
  * the tensor-core path when K >= 64 and N >= 32.  Shapes neither kernel
