@@ -668,9 +668,12 @@ def main():
     if rank == 0 and not args.no_cpu_baseline:
         us, desc, made = time_oracle(res["inp"], 12.0, 8, ex=res["ex"], with_align=not args.naive)
         cpu = {"value": us, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": desc}
-        us_t, desc_t, nt = time_oracle_threads(res["inp"], 4.0, 8, host_threads(), ex=res["ex"],
-                                               with_align=not args.naive)
-        cpu_threads = {"value": us_t, "unit": "us/call", "cores": nt, "kind": "oracle", "sample": desc_t}
+        try:
+            us_t, desc_t, nt = time_oracle_threads(res["inp"], 4.0, 8, host_threads(), ex=res["ex"],
+                                                   with_align=not args.naive)
+            cpu_threads = {"value": us_t, "unit": "us/call", "cores": nt, "kind": "oracle", "sample": desc_t}
+        except Exception as exc:   # a secondary baseline: reported, never fatal to the line
+            cpu_threads = {"value": None, "error": "%s: %s" % (type(exc).__name__, exc)}
     if rank != 0:
         if pg is not None:
             pg.destroy_process_group()

@@ -117,3 +117,26 @@ def test_forced_align_variant_is_named_in_the_config(monkeypatch, v, name):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--align-variant", str(v)])
     cfg = bench.ex_config(bench.parse())
     assert cfg.get("align_variant") == name
+
+
+def test_a_failing_threaded_baseline_does_not_lose_the_line(monkeypatch, capsys, tiny):
+    import json
+    import sys
+    counts = bench.algorithmic_counts(tiny)
+
+    def fake_run(args, world, rank, local, pg):
+        return dict(ms=2.0, clocks={}, fused_us=1.5, align_us=0.5, counts=counts, NB=8, l2=1, footprint=1,
+                    kernel_name="fused_cuda_core_kernel", align_launches=1, e2e=None, achieved=1.0, peak=2.0,
+                    peak_kind="measured", inp=tiny, ex=None)
+
+    def boom(*a, **k):
+        raise RuntimeError("threaded oracle run differs from the single-threaded one")
+
+    monkeypatch.setattr(bench, "run_ours", fake_run)
+    monkeypatch.setattr(bench, "time_oracle", lambda inp, b, n, ex=None, with_align=True: (5.0, "s1", 1))
+    monkeypatch.setattr(bench, "time_oracle_threads", boom)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "tiny", "--steps", "4", "--warmup", "3"])
+    bench.main()
+    d = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert d["cpu_baseline"]["value"] == 5.0
+    assert d["cpu_baseline_threads"]["value"] is None and "differs" in d["cpu_baseline_threads"]["error"]
