@@ -2,16 +2,23 @@
 
 One step = one pass of the whole path over one batch: moe_lora_align followed
 by moe_lora_fused_shrink_expand (add_inputs=1).  The metric is microseconds
-per step (lower is better); the default workload is the decode Qwen3-MoE-30B-A3B
-w13 LoRA shape (M=16, K=2048, N=1536, E=128, topk=8, max_loras=4 with 2
-active, r=16, block_size=16, Zipf(1.1) routing), inputs synthetic and seeded.
+per step (lower is better).  The headline workload is the largest
+configuration of the specification, large_e_nact8 (M=4096, K=7168, N=4096,
+E=256, topk=8, max_loras=8 all active, r=128, block_size=64, Zipf(1.2)
+routing); inputs are synthetic and seeded.  The same run measures every other
+configuration (tiny, decode Qwen3, decode gpt-oss, prefill Mixtral, large E
+with 1 and 4 active adapters) and reports each under "configs": fused and
+align microseconds (both align variants forced as well), the step, GB/s,
+TFLOP/s and the fractions of the measured HBM and bf16 peaks.
 
 Timing: inputs are resident in HBM; NB rotating copies of every input whose
 total footprint exceeds 3x L2 are cycled so that no step finds its operands in
-L2; W untimed warm-up steps; then exactly K steps replayed from CUDA graphs,
-bracketed by a barrier and a device synchronisation, timed with CUDA events on
-the launching stream; the max over ranks is reported.  Kernel-level durations
-(align alone, fused alone) are taken the same way for the roofline entry.
+L2; W untimed warm-up steps; then timed regions of exactly K steps each,
+replayed from CUDA graphs, each bracketed by a barrier and a device
+synchronisation and timed with CUDA events on the launching stream (max over
+ranks).  Regions are repeated (at least 5, and until they add up to 0.5 s of
+device time) and the median is reported.  Kernel-level durations (align
+alone, fused alone) are taken the same way for the roofline entry.
 
 Launch under torchrun for N > 1: every rank runs its own replica (the path has
 no exchange step); rank 0 prints the JSON line.
@@ -43,7 +50,7 @@ if ROOT not in sys.path:
 
 from lora_moe_gb300 import inputs as gen  # noqa: E402
 
-DEFAULT_WORKLOAD = "decode_qwen3_w13"
+DEFAULT_WORKLOAD = "large_e_nact8"
 METRIC = "fused MoE-LoRA us/call (align + fused shrink/expand step)"
 
 
@@ -69,6 +76,12 @@ def parse():
     ap.add_argument("--routed-weight", action="store_true", help="scale by the router weight (general call)")
     ap.add_argument("--naive", action="store_true",
                     help="naive block assignment: the step is the fused call alone, one work item per pair")
+    ap.add_argument("--configs", default="all", choices=["all", "none"],
+                    help="also measure every configuration of the specification (per-config entries)")
+    ap.add_argument("--min-regions", type=int, default=5, help="fewest timed K-step regions (median reported)")
+    ap.add_argument("--min-timed-seconds", type=float, default=0.5,
+                    help="timed regions are repeated until they add up to this much device time")
+    ap.add_argument("--max-regions", type=int, default=200)
     return ap.parse_args()
 
 
@@ -135,14 +148,26 @@ NCU_TRAFFIC = {
 }
 
 
+def _peaks_file():
+    with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+        return json.load(fh)
+
+
 def measured_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    """HBM copy bandwidth (GB/s): the measured figure, else the fallback."""
     try:
-        with open(path) as fh:
-            d = json.load(fh)
-        return float(d["hbm_gbs"]), "measured"
+        return float(_peaks_file()["hbm_gbs"]), "measured"
     except Exception:
         return 6800.0, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 tensor throughput (TFLOP/s) for a kernel timed alone: the
+    measured burst figure, else the fallback."""
+    try:
+        return float(_peaks_file()["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 # --------------------------------------------------------------------------- clocks
@@ -364,6 +389,181 @@ def time_oracle_threads(inp: gen.Inputs, budget_s: float, pairs_per_thread: int,
 
 # --------------------------------------------------------------------------- GPU side
 
+# The workloads of the per-config entries, in the order the specification
+# lists them (tiny, decode Qwen3, decode gpt-oss, prefill Mixtral, large E
+# with 1 / 4 / 8 active adapters).
+CONFIG_WORKLOADS = ["tiny", "decode_qwen3_w13", "decode_gptoss_w2", "prefill_mixtral_w13",
+                    "large_e_nact1", "large_e_nact4", "large_e_nact8"]
+
+
+class Rig:
+    """NB rotating device copies of one workload's inputs (enough that their
+    total footprint exceeds 3x L2), their align buffers, and the two calls of
+    a step on them."""
+
+    def __init__(self, w, args, dev, stream, err, inp=None, ex=None):
+        import torch
+        from lora_moe_gb300 import binding as B
+        self.B, self.w, self.args, self.dev, self.stream, self.err = B, w, args, dev, stream, err
+        if inp is None:
+            inp, ex = make_step_inputs(w, args)
+        self.inp, self.ex = inp, ex
+        src = ex if ex is not None else inp
+        self.src = src
+        a_list = src.lora_a if ex is not None else [inp.lora_a]
+        b_list = src.lora_b if ex is not None else [inp.lora_b]
+
+        def i32(a):
+            return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
+
+        def bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.per_set = (src.x.nbytes + sum(a.nbytes for a in a_list) + sum(b.nbytes for b in b_list) +
+                        2 * src.y_in.nbytes + inp.topk_ids.nbytes + inp.token_lora_mapping.nbytes)
+        self.NB = args.sets if args.sets > 0 else int(max(2, min(64, -(-3 * self.l2 // self.per_set))))
+        base = dict(topk_ids=i32(inp.topk_ids), mapping=i32(inp.token_lora_mapping), lora_ids=i32(inp.lora_ids),
+                    x=bf16(src.x), y=bf16(src.y_in))
+        self.adapter_keys = []
+        for i, (a, b) in enumerate(zip(a_list, b_list)):
+            base["a%d" % i] = bf16(a)
+            base["b%d" % i] = bf16(b)
+            self.adapter_keys += ["a%d" % i, "b%d" % i]
+        if ex is not None and ex.topk_weights is not None:
+            base["w"] = torch.from_numpy(ex.topk_weights).to(dev)
+        self.sets = []
+        for i in range(self.NB):
+            s = {k: v.clone() for k, v in base.items()}
+            s["buf"] = self.new_buffers()
+            self.sets.append(s)
+        del base
+        self.align_launches = 0 if args.naive else self.launches_of(args.align_variant)
+
+    def new_buffers(self):
+        w = self.w
+        # a workspace large enough for either variant, so that any variant can be forced
+        return self.B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size,
+                                   device=self.dev, variant=self.B.ALIGN_GLOBAL)
+
+    def launches_of(self, variant):
+        w = self.w
+        ws = self.B.align_workspace_bytes(w.M, w.topk, w.E, w.num_active_loras, w.block_size, variant)
+        return 3 if ws else 1
+
+    def align(self, s, variant=None):
+        w, b = self.w, s["buf"]
+        self.B.moe_lora_align(s["topk_ids"], s["mapping"], s["lora_ids"], w.E, w.max_loras, w.block_size,
+                              b.sorted_token_ids, b.expert_ids, b.num_tokens_post_padded, workspace=b.workspace,
+                              variant=self.args.align_variant if variant is None else variant, err_flag=self.err,
+                              stream=self.stream)
+
+    def fused(self, s):
+        w, b, args, ex, B = self.w, s["buf"], self.args, self.ex, self.B
+        S = args.slices
+        if args.naive:
+            B.moe_lora_fused_shrink_expand_naive(
+                s["x"], [s["a%d" % i] for i in range(S)], [s["b%d" % i] for i in range(S)],
+                s["y"], s["topk_ids"], s["mapping"], s["lora_ids"], w.max_loras, add_inputs=True,
+                topk_weights=s.get("w"), x_per_pair=ex.x_per_pair, y_offset=ex.y_offset, err_flag=self.err,
+                stream=self.stream)
+        elif ex is None:
+            B.moe_lora_fused_shrink_expand(s["x"], s["a0"], s["b0"], s["y"], b.sorted_token_ids, b.expert_ids,
+                                           b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
+                                           add_inputs=True, path=args.path, err_flag=self.err, stream=self.stream)
+        else:
+            B.moe_lora_fused_shrink_expand_ex(
+                s["x"], [s["a%d" % i] for i in range(S)], [s["b%d" % i] for i in range(S)],
+                s["y"], b.sorted_token_ids, b.expert_ids, b.num_tokens_post_padded, s["lora_ids"], w.topk,
+                w.block_size, add_inputs=True, topk_weights=s.get("w"), x_per_pair=ex.x_per_pair,
+                y_offset=ex.y_offset, path=args.path, err_flag=self.err, stream=self.stream)
+
+    def step(self, i):
+        s = self.sets[i % self.NB]
+        if not self.args.naive:
+            self.align(s)
+        self.fused(s)
+
+    def capture(self, fn, n):
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(self.stream):
+            with torch.cuda.graph(g, stream=self.stream):
+                for i in range(n):
+                    fn(i)
+        return g
+
+    def graph_time_us(self, fn, seconds):
+        """Microseconds per call of fn, replayed from a graph of NB calls (one
+        per input set) for about `seconds` of device time."""
+        import torch
+        g = self.capture(lambda i: fn(self.sets[i % self.NB]), self.NB)
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        st = self.stream
+        with torch.cuda.stream(st):
+            g.replay()
+            st.synchronize()
+            a.record(st)
+            g.replay()
+            b.record(st)
+            st.synchronize()
+            one = max(1e-6, a.elapsed_time(b))
+            reps = max(1, int(seconds * 1e3 / one))
+            a.record(st)
+            for _ in range(reps):
+                g.replay()
+            b.record(st)
+            st.synchronize()
+        del g
+        return a.elapsed_time(b) * 1e3 / (reps * self.NB)
+
+    def check_err(self):
+        v = int(self.err.item())
+        assert v == 0, "device error flag %d" % v
+
+    def release(self):
+        import torch
+        self.sets = []
+        torch.cuda.empty_cache()
+
+
+def kernel_name_of(B, w, args):
+    kernel = B.fused_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size,
+                                  args.slices, args.path)
+    name = {B.PATH_TCGEN05: "fused_tcgen05_kernel", B.PATH_CUDA_CORE_CLUSTER: "fused_cuda_core_kernel",
+            B.PATH_CUDA_CORE_STREAM: "fused_stream_cc_kernel"}[kernel]
+    if args.naive:
+        name = "fused_cuda_core_kernel (naive block assignment)"
+    return name
+
+
+def config_entry(rig, counts, peak, tc_peak, seconds):
+    """Per-config numbers, each kernel alone and the align + fused step, all
+    from CUDA graphs over the rotating input sets."""
+    B, w = rig.B, rig.w
+    for i in range(max(3, rig.NB)):
+        rig.step(i)
+    rig.stream.synchronize()
+    rig.check_err()
+    fused_us = rig.graph_time_us(rig.fused, seconds)
+    align = {}
+    if not rig.args.naive:
+        align["align_us"] = rig.graph_time_us(rig.align, seconds)
+        align["align_us_smem"] = rig.graph_time_us(lambda s: rig.align(s, B.ALIGN_SMEM), seconds)
+        align["align_us_global"] = rig.graph_time_us(lambda s: rig.align(s, B.ALIGN_GLOBAL), seconds)
+        align["align_variant_auto"] = "global" if rig.launches_of(B.ALIGN_AUTO) == 3 else "smem"
+    step_us = rig.graph_time_us(lambda s: (rig.align(s) if not rig.args.naive else None, rig.fused(s)), seconds)
+    rig.check_err()
+    gbs = counts["fused_bytes"] / (fused_us * 1e-6) / 1e9
+    tflops = counts["flops"] / (fused_us * 1e-6) / 1e12
+    return dict({"kernel": kernel_name_of(B, w, rig.args), "step_us": step_us, "fused_us": fused_us,
+                 "fused_gbs": gbs, "fused_tflops": tflops, "frac_hbm": gbs / peak,
+                 "frac_bf16_tensor": tflops / tc_peak,
+                 "fused_bytes": counts["fused_bytes"], "flops": counts["flops"], "pairs": counts["pairs"],
+                 "blocks": counts["blocks"]}, **align)
+
+
 def run_ours(args, world, rank, local, pg):
     import torch
     from lora_moe_gb300 import binding as B
@@ -371,148 +571,65 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = gen.WORKLOADS[args.workload]
-    inp, ex = make_step_inputs(w, args)
-    counts = algorithmic_counts(inp, args.slices, args.per_pair_x, args.routed_weight, args.naive)
-
-    def i32(a):
-        return torch.from_numpy(np.ascontiguousarray(a, np.int32)).to(dev)
-
-    def bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
-
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    src = ex if ex is not None else inp
-    a_list = src.lora_a if ex is not None else [inp.lora_a]
-    b_list = src.lora_b if ex is not None else [inp.lora_b]
-    per_set = (src.x.nbytes + sum(a.nbytes for a in a_list) + sum(b.nbytes for b in b_list) + 2 * src.y_in.nbytes +
-               inp.topk_ids.nbytes + inp.token_lora_mapping.nbytes)
-    NB = args.sets if args.sets > 0 else int(max(2, min(64, -(-3 * l2 // per_set))))
-    base = dict(topk_ids=i32(inp.topk_ids), mapping=i32(inp.token_lora_mapping), lora_ids=i32(inp.lora_ids),
-                x=bf16(src.x), y=bf16(src.y_in))
-    base_keys_adapters = []
-    for i, (a, b) in enumerate(zip(a_list, b_list)):
-        base["a%d" % i] = bf16(a)
-        base["b%d" % i] = bf16(b)
-        base_keys_adapters += ["a%d" % i, "b%d" % i]
-    if ex is not None and ex.topk_weights is not None:
-        base["w"] = torch.from_numpy(ex.topk_weights).to(dev)
-    sets = []
-    for i in range(NB):
-        s = {k: v.clone() for k, v in base.items()}
-        s["buf"] = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size, device=dev,
-                                  variant=args.align_variant)
-        sets.append(s)
-    del base
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(device=dev)
-    variant_ws = sets[0]["buf"].workspace is not None
-    align_launches = 3 if variant_ws else 1
-
-    def align(s):
-        b = s["buf"]
-        B.moe_lora_align(s["topk_ids"], s["mapping"], s["lora_ids"], w.E, w.max_loras, w.block_size,
-                         b.sorted_token_ids, b.expert_ids, b.num_tokens_post_padded, workspace=b.workspace,
-                         variant=args.align_variant, err_flag=err, stream=stream)
-
-    def fused(s):
-        b = s["buf"]
-        if args.naive:
-            B.moe_lora_fused_shrink_expand_naive(
-                s["x"], [s["a%d" % i] for i in range(args.slices)], [s["b%d" % i] for i in range(args.slices)],
-                s["y"], s["topk_ids"], s["mapping"], s["lora_ids"], w.max_loras, add_inputs=True,
-                topk_weights=s.get("w"), x_per_pair=ex.x_per_pair, y_offset=ex.y_offset, err_flag=err,
-                stream=stream)
-        elif ex is None:
-            B.moe_lora_fused_shrink_expand(s["x"], s["a0"], s["b0"], s["y"], b.sorted_token_ids, b.expert_ids,
-                                           b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
-                                           add_inputs=True, path=args.path, err_flag=err, stream=stream)
-        else:
-            B.moe_lora_fused_shrink_expand_ex(
-                s["x"], [s["a%d" % i] for i in range(args.slices)], [s["b%d" % i] for i in range(args.slices)],
-                s["y"], b.sorted_token_ids, b.expert_ids, b.num_tokens_post_padded, s["lora_ids"], w.topk,
-                w.block_size, add_inputs=True, topk_weights=s.get("w"), x_per_pair=ex.x_per_pair,
-                y_offset=ex.y_offset, path=args.path, err_flag=err, stream=stream)
-
-    def step(i):
-        s = sets[i % NB]
-        if not args.naive:
-            align(s)
-        fused(s)
+    rig = Rig(w, args, dev, stream, err)
+    inp, ex = rig.inp, rig.ex
+    counts = algorithmic_counts(inp, args.slices, args.per_pair_x, args.routed_weight, args.naive)
+    NB = rig.NB
 
     if args.profile_steps:
         with torch.cuda.stream(stream):
             for i in range(args.warmup + args.profile_steps):
-                step(i)
+                rig.step(i)
         stream.synchronize()
-        assert int(err.item()) == 0, "device error flag %d" % int(err.item())
+        rig.check_err()
         return None
-
-    def capture(fn, n):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(stream):
-            with torch.cuda.graph(g, stream=stream):
-                for i in range(n):
-                    fn(i)
-        return g
 
     # warm-up (also primes every set's align output for the fused-only timing)
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, NB)):
-            step(i)
+            rig.step(i)
     stream.synchronize()
-    assert int(err.item()) == 0, "device error flag %d" % int(err.item())
+    rig.check_err()
 
-    g_round = capture(step, NB)
+    g_round = rig.capture(rig.step, NB)
     rem = args.steps % NB
-    g_rem = capture(step, rem) if rem else None
+    g_rem = rig.capture(rig.step, rem) if rem else None
     stream.synchronize()
 
-    # ---------------- timed region: exactly K steps
+    # ---------------- timed regions: each exactly K steps; the median is reported
+    def timed_region():
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        barrier(pg, True)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps // NB):
+                g_round.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            e1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        barrier(pg, True)
+        return max_over_ranks(pg, e0.elapsed_time(e1), True)
+
     sampler = ClockSampler(local)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    barrier(pg, True)
-    torch.cuda.synchronize()
     sampler.start()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps // NB):
-            g_round.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        e1.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
-    barrier(pg, True)
+    regions = [timed_region()]
+    want = max(args.min_regions, int(np.ceil(args.min_timed_seconds * 1e3 / max(1e-6, regions[0]))))
+    while len(regions) < min(want, args.max_regions):
+        regions.append(timed_region())
     clocks = sampler.stop()
-    _, ms = job_us_per_step(pg, e0.elapsed_time(e1), args.steps, world, True)
-    assert int(err.item()) == 0, "device error flag %d" % int(err.item())
+    rig.check_err()
+    ms = float(np.median(regions))
 
     # ---------------- kernel-level timing (each kernel alone, same rotation)
-    def kernel_time(fn, launches_per_call):
-        g = capture(lambda i: fn(sets[i % NB]), NB)
-        a = torch.cuda.Event(enable_timing=True)
-        b = torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            g.replay()
-            stream.synchronize()
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            stream.synchronize()
-            one = max(1e-6, a.elapsed_time(b))
-            reps = max(1, int(args.kernel_seconds * 1e3 / one))
-            a.record(stream)
-            for _ in range(reps):
-                g.replay()
-            b.record(stream)
-            stream.synchronize()
-        return a.elapsed_time(b) * 1e3 / (reps * NB)   # us per call
-
-    fused_us = kernel_time(fused, 1)
-    align_us = None if args.naive else kernel_time(align, align_launches)
-    if args.naive:
-        align_launches = 0
+    fused_us = rig.graph_time_us(rig.fused, args.kernel_seconds)
+    align_us = None if args.naive else rig.graph_time_us(rig.align, args.kernel_seconds)
+    align_launches = rig.align_launches
 
     # ---------------- end to end through the public API with host buffers
     # Each step's inputs (routing, x, y_in, router weights) sit in one pinned
@@ -520,6 +637,7 @@ def run_ours(args, world, rank, local, pg):
     # take: one host-to-device copy per step, the two calls, and y read back.
     e2e = None
     if not args.no_e2e:
+        src = rig.src
         parts = [("topk_ids", inp.topk_ids), ("mapping", inp.token_lora_mapping), ("lora_ids", inp.lora_ids),
                  ("x", src.x), ("y", src.y_in)]
         if ex is not None and ex.topk_weights is not None:
@@ -539,23 +657,23 @@ def run_ours(args, world, rank, local, pg):
             v = {"pack": dev_pack}
             for name, (off, arr) in layout.items():
                 v[name] = dev_pack[off:off + arr.nbytes].view(tdt[name]).view(arr.shape)
-            for name in base_keys_adapters:
-                v[name] = sets[0][name]
+            for name in rig.adapter_keys:
+                v[name] = rig.sets[0][name]
             v["buf"] = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size,
                                       device=dev, variant=args.align_variant)
             packs.append(v)
         out_host = torch.empty(src.y_in.shape, dtype=torch.int16).pin_memory()
         h2d = total
         d2h = out_host.numel() * out_host.element_size()
-        n_e2e = max(3, min(args.steps, 2000))
+        n_e2e = max(4, min(args.steps, 2000))
 
         def e2e_step(i):
             v = packs[i % 2]
             with torch.cuda.stream(stream):
                 v["pack"].copy_(host_pack, non_blocking=True)
             if not args.naive:
-                align(v)
-            fused(v)
+                rig.align(v)
+            rig.fused(v)
             with torch.cuda.stream(stream):
                 out_host.copy_(v["y"].view(torch.int16), non_blocking=True)
 
@@ -575,8 +693,8 @@ def run_ours(args, world, rank, local, pg):
         # The same steps captured in a CUDA graph (the way serving engines run
         # decode steps): every replayed step still copies its inputs from
         # pinned host memory, runs the calls and reads y back to the host.
-        g_e2e = capture(e2e_step, 2)
-        reps = max(1, n_e2e // 2)
+        g_e2e = rig.capture(e2e_step, 2)
+        reps = max(2, n_e2e // 2)
         with torch.cuda.stream(stream):
             g_e2e.replay()
         stream.synchronize()
@@ -589,24 +707,41 @@ def run_ours(args, world, rank, local, pg):
         b.record(stream)
         stream.synchronize()
         graph_ms = max_over_ranks(pg, a.elapsed_time(b), True)
+        rig.check_err()
         e2e = {"value": graph_ms * 1e3 / (reps * 2 * world), "unit": "us/call", "steps": reps * 2,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "mode": "CUDA graph of each step's host-to-device copy of its packed inputs, the calls and the "
                        "read-back of y",
                "eager_value": eager_ms * 1e3 / (n_e2e * world)}
+        del packs, g_e2e
 
     peak, peak_kind = measured_peaks()
+    tc_peak, tc_kind = measured_tensor_peak()
     achieved = counts["fused_bytes"] / (fused_us * 1e-6) / 1e9
-    kernel = B.fused_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size,
-                                  args.slices, args.path)
-    kernel_name = {B.PATH_TCGEN05: "fused_tcgen05_kernel", B.PATH_CUDA_CORE_CLUSTER: "fused_cuda_core_kernel",
-                   B.PATH_CUDA_CORE_STREAM: "fused_stream_cc_kernel"}[kernel]
-    if args.naive:
-        kernel_name = "fused_cuda_core_kernel (naive block assignment)"
-    return dict(ms=ms, clocks=clocks, fused_us=fused_us, align_us=align_us, counts=counts, NB=NB, l2=l2,
-                footprint=NB * per_set, kernel_name=kernel_name,
-                align_launches=align_launches, e2e=e2e, achieved=achieved, peak=peak, peak_kind=peak_kind,
-                inp=inp, ex=ex)
+    kernel_name = kernel_name_of(B, w, args)
+    res = dict(ms=ms, regions=regions, clocks=clocks, fused_us=fused_us, align_us=align_us, counts=counts, NB=NB,
+               l2=rig.l2, footprint=NB * rig.per_set, kernel_name=kernel_name, align_launches=align_launches,
+               e2e=e2e, achieved=achieved, peak=peak, peak_kind=peak_kind, tc_peak=tc_peak, tc_kind=tc_kind,
+               inp=inp, ex=ex)
+    del g_round, g_rem
+
+    # ---------------- the other configurations, measured in the same run
+    configs = {}
+    if args.configs == "all" and not uses_ex(args) and args.path == 0 and args.align_variant == 0:
+        configs[w.name] = config_entry(rig, counts, peak, tc_peak, args.kernel_seconds)
+        rig.release()
+        del rig
+        for name in CONFIG_WORKLOADS:
+            if name == w.name:
+                continue
+            wc = gen.WORKLOADS[name]
+            r2 = Rig(wc, args, dev, stream, err)
+            c2 = algorithmic_counts(r2.inp)
+            configs[name] = config_entry(r2, c2, peak, tc_peak, args.kernel_seconds)
+            r2.release()
+            del r2
+    res["configs"] = configs
+    return res
 
 
 def ex_config(args):
@@ -678,6 +813,9 @@ def main():
         if pg is not None:
             pg.destroy_process_group()
         return
+    regions = res["regions"]
+    launches_per_step = res["align_launches"] + 1
+    tflops = counts["flops"] / (res["fused_us"] * 1e-6) / 1e12
     line = {
         "metric": METRIC, "value": us_per_step, "unit": "us/call", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": res["ms"] / args.steps, "higher_is_better": False,
@@ -688,12 +826,16 @@ def main():
                    "block_size": w.block_size, "add_inputs": 1, "parallelism": "replicas" if world > 1 else "single",
                    "l2_policy": "%d rotating input sets, %.0f MB in total, L2 %.0f MB" % (
                        res["NB"], res["footprint"] / 1e6, res["l2"] / 1e6),
-                   "timing": "CUDA graphs of align+fused steps, CUDA events on the launching stream",
+                   "timing": ("median of %d timed regions of exactly %d align+fused steps each (CUDA graphs, CUDA "
+                              "events on the launching stream, barrier and device synchronisation around each "
+                              "region, max over ranks)" % (len(regions), args.steps)),
                    **ex_config(args)},
+        "timed_regions": {"count": len(regions), "ms_min": min(regions), "ms_median": float(np.median(regions)),
+                          "ms_max": max(regions)},
         "kernels": {"align_us": res["align_us"], "fused_us": res["fused_us"],
                     "align_launches_per_call": res["align_launches"],
-                    "fused_gbs": res["achieved"],
-                    "fused_tflops": counts["flops"] / (res["fused_us"] * 1e-6) / 1e12,
+                    "fused_gbs": res["achieved"], "fused_tflops": tflops,
+                    "fused_frac_bf16_tensor": tflops / res["tc_peak"],
                     "align_gbs": (counts["align_bytes"] / (res["align_us"] * 1e-6) / 1e9
                                   if res["align_us"] else None)},
         "algorithmic": counts,
@@ -702,10 +844,17 @@ def main():
                      "frac": res["achieved"] / res["peak"], "peak_kind": res["peak_kind"] + " (hbm_gbs)",
                      "traffic": None if uses_ex(args) else NCU_TRAFFIC.get((w.name, res["kernel_name"])),
                      "traffic_unit": "bytes per launch (ncu)"},
+        "configs": res["configs"],
+        "configs_note": ("each configuration alone: fused_us / align_us (library's variant) / align_us_smem / "
+                         "align_us_global per call and step_us per align+fused step, from CUDA graphs over "
+                         "rotating input sets larger than 3x L2; frac_hbm = fused algorithmic bytes / fused_us / "
+                         "measured HBM copy bandwidth (%.1f GB/s); frac_bf16_tensor = flops / fused_us / "
+                         "measured bf16 burst (%.1f TFLOP/s, %s)" % (res["peak"], res["tc_peak"], res["tc_kind"])),
         "cpu_baseline": cpu,
         "cpu_baseline_threads": cpu_threads,
         "e2e": res["e2e"],
-        "gpu_launches": args.steps * (res["align_launches"] + 1),
+        "gpu_launches": args.steps * launches_per_step,
+        "gpu_launches_note": "per timed region (%d launches per step)" % launches_per_step,
         "clocks": res["clocks"],
     }
     print(json.dumps(line))

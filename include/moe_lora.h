@@ -348,13 +348,16 @@ int moe_lora_fused_plan(int M, int topk, int num_experts, int K, int N, int rank
  * buffer compiled into the library (every GPU that loads the library holds it
  * until the process exits).  Nothing is allocated by this call.
  *   - Same arguments, results and errors as moe_lora_align with
- *     variant = MOE_LORA_ALIGN_GLOBAL, minus the workspace arguments.
- *   - Returns MOE_LORA_ERR_WORKSPACE when
+ *     variant = MOE_LORA_ALIGN_GLOBAL, minus the workspace arguments.  Those
+ *     argument checks come first; then it returns MOE_LORA_ERR_WORKSPACE when
  *     moe_lora_align_workspace_bytes(M, topk, num_experts, num_active_loras,
  *     block_size, MOE_LORA_ALIGN_GLOBAL) exceeds MOE_LORA_STATIC_WORKSPACE_BYTES.
- *   - The first call on each device (with that device current) looks up the
- *     buffer's device address; make that first call before any stream capture.
- *   - All calls on a device share the one buffer, which keeps the last call's
+ *   - The first call in each CUDA context (normally once per device, in the
+ *     runtime's primary context), with that context current, looks up the
+ *     buffer's device address; make that first call before any stream
+ *     capture.  A new context (after cudaDeviceReset, or a caller's own
+ *     driver context) gets a lookup of its own on its first call.
+ *   - All calls in a context share the one buffer, which keeps the last call's
  *     contents (no entry needs clearing between calls).  Calls that overlap on
  *     the GPU -- on different streams, or from host threads without ordering
  *     between them -- race on it and must not be issued.

@@ -217,6 +217,27 @@ static int resolve_path(const FusedArgs &f, int path, size_t max_smem) {
   return use;
 }
 
+namespace moe_lora {
+
+int check_align_args(const int32_t *topk_ids, const int32_t *token_lora_mapping, const int32_t *lora_ids, int M,
+                     int topk, int num_experts, int max_loras, int num_active_loras, int block_size,
+                     const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                     const int32_t *num_tokens_post_padded, int max_num_tokens_padded, int max_num_m_blocks,
+                     int variant) {
+  if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
+                            max_num_m_blocks))
+    return st;
+  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_GLOBAL) return MOE_LORA_ERR_INVALID_ARG;
+  if (M > 0 && num_active_loras > 0 && !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_active_loras > 0 && !lora_ids) return MOE_LORA_ERR_INVALID_ARG;
+  if (num_active_loras == 0) return MOE_LORA_OK;
+  if (!sorted_token_ids || !expert_ids || !num_tokens_post_padded) return MOE_LORA_ERR_INVALID_ARG;
+  if (M > 0 && !topk_ids) return MOE_LORA_ERR_INVALID_ARG;
+  return MOE_LORA_OK;
+}
+
+}  // namespace moe_lora
+
 extern "C" {
 
 int moe_lora_version(void) { return 100; }
@@ -260,12 +281,10 @@ int moe_lora_align(const int32_t *topk_ids, const int32_t *token_lora_mapping, c
                    int num_active_loras, int block_size, int32_t *sorted_token_ids, int32_t *expert_ids,
                    int32_t *num_tokens_post_padded, int max_num_tokens_padded, int max_num_m_blocks,
                    void *workspace, size_t workspace_bytes, int variant, int32_t *err_flag, void *stream) {
-  if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
-                            max_num_m_blocks))
+  if (int st = check_align_args(topk_ids, token_lora_mapping, lora_ids, M, topk, num_experts, max_loras,
+                                num_active_loras, block_size, sorted_token_ids, expert_ids, num_tokens_post_padded,
+                                max_num_tokens_padded, max_num_m_blocks, variant))
     return st;
-  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_GLOBAL) return MOE_LORA_ERR_INVALID_ARG;
-  if (M > 0 && num_active_loras > 0 && !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
-  if (num_active_loras > 0 && !lora_ids) return MOE_LORA_ERR_INVALID_ARG;
   return align_impl(topk_ids, token_lora_mapping, lora_ids, adapter_enabled, M, topk, num_experts, max_loras,
                     num_active_loras, block_size, sorted_token_ids, expert_ids, num_tokens_post_padded,
                     max_num_tokens_padded, max_num_m_blocks, workspace, workspace_bytes, variant, err_flag, stream);

@@ -82,6 +82,14 @@ int align_global_pairs_per_warp(int M, int topk);
 size_t align_global_workspace_bytes(int M, int topk, int E, int nact);
 bool align_smem_fits(int E);
 
+// The argument checks of moe_lora_align (sizes, variant, required pointers),
+// without touching a device: 0 or a moe_lora_status code.
+int check_align_args(const int32_t *topk_ids, const int32_t *token_lora_mapping, const int32_t *lora_ids, int M,
+                     int topk, int num_experts, int max_loras, int num_active_loras, int block_size,
+                     const int32_t *sorted_token_ids, const int32_t *expert_ids,
+                     const int32_t *num_tokens_post_padded, int max_num_tokens_padded, int max_num_m_blocks,
+                     int variant);
+
 int launch_align_smem(const AlignArgs &a, cudaStream_t stream);
 int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream);
 int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream);

@@ -9,19 +9,26 @@ Workloads are shaped like the models the vLLM pages benchmark (vLLM PR #29257
 "[LoRA] Support FusedMoE LoRA Triton kernel for mxfp4", gpt-oss-20b serving
 run; the prhub.com.cn summary of vLLM PR #42290, section "Implementation
 breakdown", step 4, which benchmarks qwen3moe-shaped inputs).  No dataset or
-trained weight is used: every value is drawn from numpy's PCG64 generator
-(`numpy.random.default_rng(seed)`) in a fixed order:
+trained weight is used: every value comes from numpy's PCG64 generator.
 
-    active LoRA set -> topk_ids -> token_lora_mapping -> x -> A -> B -> y_in
+Routing is drawn from one stream, `numpy.random.default_rng(seed)`, in the
+order
+
+    active LoRA set -> topk_ids -> token_lora_mapping
+
+Tensors are drawn in chunks of 2**24 elements, chunk c of a tensor from its
+own stream `numpy.random.default_rng([seed, tag, slice, slot, c])`, so that
+the value of every element is fixed by definition whatever the tensor size,
+and chunks can be drawn on several host threads at once.  Tags: 1 x,
+2 A, 3 B, 4 y_in, 5 x with one row per pair, 6 a wide y_in (output offset or
+row stride); `slice` is the adapter slice (0 for the plain call) and `slot`
+the LoRA slot of an adapter (0 for x and y_in).  Router weights come from
+`default_rng([seed, 7])`.
 
 Value distributions: x ~ N(0,1); A[l,e] ~ N(0, 1/K) (K = input dim of the
-adapter); B[l,e] ~ N(0, 1/r); y_in ~ N(0,1).  The options of the general fused
-call (make_ex_inputs) draw from a second stream, seeded [seed, 1], in the order
-
-    x per pair -> A and B of slices 1.. -> router weights -> wide y_in
-
-with router weights a softmax over each token's top-k of N(0,1) draws (float32,
-positive, summing to 1 per token, like a router's top-k probabilities).  Normals are drawn as float32 and
+adapter); B[l,e] ~ N(0, 1/r); y_in ~ N(0,1); router weights a softmax over
+each token's top-k of N(0,1) draws (float32, positive, summing to 1 per token,
+like a router's top-k probabilities).  Normals are drawn as float32 and
 rounded to bf16 with round-to-nearest-even.  Adapter slots that are not in the
 active set are filled with a bf16 quiet NaN (0x7FC0) so that any read of an
 inactive slot shows up in the output.
@@ -30,14 +37,17 @@ bf16 values are carried as numpy uint16 arrays holding the raw bit patterns.
 """
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
+import os
+import threading
 from typing import Optional
 
 import numpy as np
 
 BF16_QNAN = np.uint16(0x7FC0)
-# Draws are made in chunks of this many elements so that the stream of
-# random numbers is fixed by definition, whatever the tensor size.
+# Tensors are drawn in chunks of this many elements, each chunk from its own
+# keyed stream.
 _CHUNK = 1 << 24
 
 
@@ -123,15 +133,74 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
-def _normal_bf16(rng: np.random.Generator, n: int, scale: float) -> np.ndarray:
-    out = np.empty(n, dtype=np.uint16)
-    for s in range(0, n, _CHUNK):
-        e = min(n, s + _CHUNK)
-        v = rng.standard_normal(e - s, dtype=np.float32)
-        if scale != 1.0:
-            v *= np.float32(scale)
-        out[s:e] = f32_to_bf16_bits(v)
+_TAG_X, _TAG_A, _TAG_B, _TAG_Y, _TAG_X_PAIR, _TAG_Y_WIDE, _TAG_WEIGHTS = 1, 2, 3, 4, 5, 6, 7
+
+_pool = None
+_pool_lock = threading.Lock()
+_scratch = threading.local()
+
+
+def _executor() -> concurrent.futures.ThreadPoolExecutor:
+    global _pool
+    with _pool_lock:
+        if _pool is None:
+            try:
+                n = len(os.sched_getaffinity(0))
+            except AttributeError:
+                n = os.cpu_count() or 1
+            _pool = concurrent.futures.ThreadPoolExecutor(max_workers=max(1, min(32, n)))
+    return _pool
+
+
+def _draw_chunk(out: np.ndarray, key, scale: float) -> None:
+    """out[:] = bf16(scale * N(0,1) draws of stream `key`), float32 draws."""
+    n = out.size
+    buf = getattr(_scratch, "f32", None)
+    if buf is None or buf.size < n:
+        buf = _scratch.f32 = np.empty(_CHUNK, np.float32)
+        _scratch.u32 = np.empty(_CHUNK, np.uint32)
+    v = buf[:n]
+    np.random.default_rng(key).standard_normal(dtype=np.float32, out=v)
+    if scale != 1.0:
+        v *= np.float32(scale)
+    # round to nearest even, in place: (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    u = v.view(np.uint32)
+    t = _scratch.u32[:n]
+    np.right_shift(u, np.uint32(16), out=t)
+    t &= np.uint32(1)
+    t += np.uint32(0x7FFF)
+    t += u
+    t >>= np.uint32(16)
+    out[...] = t
+
+
+def _normal_bf16_into(out: np.ndarray, seed: int, tag: int, sl: int, slot: int, scale: float) -> None:
+    """Fill the contiguous uint16 array `out` chunk by chunk, chunk c from the
+    stream [seed, tag, sl, slot, c] (chunks drawn on the host threads)."""
+    flat = out.reshape(-1)
+    n = flat.size
+    jobs = [_executor().submit(_draw_chunk, flat[s:min(n, s + _CHUNK)], [seed, tag, sl, slot, s // _CHUNK], scale)
+            for s in range(0, n, _CHUNK)]
+    for j in jobs:
+        j.result()
+
+
+def _normal_bf16(shape, seed: int, tag: int, sl: int, slot: int, scale: float) -> np.ndarray:
+    out = np.empty(shape, np.uint16)
+    _normal_bf16_into(out, seed, tag, sl, slot, scale)
     return out
+
+
+def _adapters(w: "Workload", lora_ids, sl: int):
+    """A [L, E, r, K] and B [L, E, N, r] of slice `sl`: N(0, 1/K) and N(0, 1/r)
+    in the listed slots, bf16 NaN elsewhere."""
+    L, E, r, K, N = w.max_loras, w.E, w.rank, w.K, w.N
+    a = np.full((L, E, r, K), BF16_QNAN, dtype=np.uint16)
+    b = np.full((L, E, N, r), BF16_QNAN, dtype=np.uint16)
+    for l in lora_ids:
+        _normal_bf16_into(a[l], w.seed, _TAG_A, sl, int(l), 1.0 / np.sqrt(K))
+        _normal_bf16_into(b[l], w.seed, _TAG_B, sl, int(l), 1.0 / np.sqrt(r))
+    return a, b
 
 
 @dataclasses.dataclass
@@ -189,15 +258,9 @@ def make_inputs(w: Workload, with_tensors: bool = True) -> Inputs:
     lora_ids, topk_ids, mapping = draw_routing(w, rng)
     if not with_tensors:
         return Inputs(w, lora_ids, topk_ids, mapping, None, None, None, None)
-    L, E, r, K, N = w.max_loras, w.E, w.rank, w.K, w.N
-    x = _normal_bf16(rng, w.M * K, 1.0).reshape(w.M, K)
-    a = np.full((L, E, r, K), BF16_QNAN, dtype=np.uint16)
-    for l in lora_ids:
-        a[l] = _normal_bf16(rng, E * r * K, 1.0 / np.sqrt(K)).reshape(E, r, K)
-    b = np.full((L, E, N, r), BF16_QNAN, dtype=np.uint16)
-    for l in lora_ids:
-        b[l] = _normal_bf16(rng, E * N * r, 1.0 / np.sqrt(r)).reshape(E, N, r)
-    y = _normal_bf16(rng, w.M * w.topk * N, 1.0).reshape(w.M, w.topk, N)
+    x = _normal_bf16((w.M, w.K), w.seed, _TAG_X, 0, 0, 1.0)
+    a, b = _adapters(w, lora_ids, 0)
+    y = _normal_bf16((w.M, w.topk, w.N), w.seed, _TAG_Y, 0, 0, 1.0)
     return Inputs(w, lora_ids, topk_ids, mapping, x, a, b, y)
 
 
@@ -218,30 +281,24 @@ class ExInputs:
 def make_ex_inputs(w: Workload, num_slices: int = 1, x_per_pair: bool = False, routed_weights: bool = False,
                    y_offset: int = 0, ldy: Optional[int] = None) -> ExInputs:
     base = make_inputs(w)
-    rng = np.random.default_rng([w.seed, 1])
-    L, E, r, K, N = w.max_loras, w.E, w.rank, w.K, w.N
+    N = w.N
     if ldy is None:
         ldy = y_offset + num_slices * N
     x = base.x
     if x_per_pair:
-        x = _normal_bf16(rng, w.M * w.topk * K, 1.0).reshape(w.M * w.topk, K)
+        x = _normal_bf16((w.M * w.topk, w.K), w.seed, _TAG_X_PAIR, 0, 0, 1.0)
     lora_a, lora_b = [base.lora_a], [base.lora_b]
-    for _ in range(1, num_slices):
-        a = np.full((L, E, r, K), BF16_QNAN, dtype=np.uint16)
-        for l in base.lora_ids:
-            a[l] = _normal_bf16(rng, E * r * K, 1.0 / np.sqrt(K)).reshape(E, r, K)
-        b = np.full((L, E, N, r), BF16_QNAN, dtype=np.uint16)
-        for l in base.lora_ids:
-            b[l] = _normal_bf16(rng, E * N * r, 1.0 / np.sqrt(r)).reshape(E, N, r)
+    for sl in range(1, num_slices):
+        a, b = _adapters(w, base.lora_ids, sl)
         lora_a.append(a)
         lora_b.append(b)
     weights = None
     if routed_weights:
-        g = rng.standard_normal((w.M, w.topk), dtype=np.float32)
+        g = np.random.default_rng([w.seed, _TAG_WEIGHTS]).standard_normal((w.M, w.topk), dtype=np.float32)
         g = np.exp(g - g.max(axis=1, keepdims=True))
         weights = (g / g.sum(axis=1, keepdims=True)).astype(np.float32)
     if ldy == N and y_offset == 0:
         y = base.y_in
     else:
-        y = _normal_bf16(rng, w.M * w.topk * ldy, 1.0).reshape(w.M, w.topk, ldy)
+        y = _normal_bf16((w.M, w.topk, ldy), w.seed, _TAG_Y_WIDE, 0, 0, 1.0)
     return ExInputs(base, x, lora_a, lora_b, weights, y, x_per_pair, y_offset)

@@ -1,5 +1,7 @@
 """Shared test helpers: move seeded inputs to the GPU, run the library's two
 stages through the binding, and compare against the CPU oracle."""
+import os
+
 import numpy as np
 import torch
 
@@ -120,3 +122,58 @@ def check_close(got_bits, ref, what=""):
         raise AssertionError("%s: %d elements out of tolerance, first at %s: got %r ref %r"
                              % (what, int(bad.sum()), tuple(i), got[tuple(i)], ref[tuple(i)]))
     return float(err.max()) if err.size else 0.0
+
+
+def host_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def as_ex(inp: gen.Inputs) -> gen.ExInputs:
+    """The plain call's inputs as general-call inputs (one slice, no options)."""
+    return gen.ExInputs(inp, inp.x, [inp.lora_a], [inp.lora_b], None, inp.y_in, False, 0)
+
+
+def compare_every_pair(ex: gen.ExInputs, outs, add_inputs=True, adapter_enabled=None, chunk=256):
+    """Compare GPU outputs with the oracle on every element.
+
+    outs: {name: uint16 [M*topk, ldy] host copy of the GPU output}.  Covered
+    pairs' slice columns must satisfy |gpu - ref| <= 1e-2 + 1e-2 |ref| against
+    the oracle's general definition; every other element (uncovered pairs, the
+    columns no slice writes) must equal y_in bit for bit.  The oracle runs on
+    chunks of `chunk` covered pairs, one chunk per host thread at a time; each
+    chunk's rows are compared with every output as soon as they are ready.
+    Returns {name: largest error}."""
+    from concurrent.futures import ThreadPoolExecutor
+    inp, w = ex.base, ex.base.w
+    P = w.M * w.topk
+    yin = ex.y_in.reshape(P, -1)
+    S = len(ex.lora_a)
+    lo, hi = ex.y_offset, ex.y_offset + S * w.N
+    cov = covered(inp, adapter_enabled).reshape(-1)
+    unc = np.flatnonzero(~cov)
+    for name, got in outs.items():
+        assert got.shape == yin.shape, name
+        assert np.array_equal(got[unc], yin[unc]), "%s: uncovered pairs were modified" % name
+        assert np.array_equal(got[:, :lo], yin[:, :lo]) and np.array_equal(got[:, hi:], yin[:, hi:]), \
+            "%s: columns outside the slices were modified" % name
+    cov_idx = np.flatnonzero(cov).astype(np.int32)
+    chunks = [cov_idx[i:i + chunk] for i in range(0, len(cov_idx), chunk)]
+
+    def work(sel):
+        ref = oracle.fused_ex(ex.x, ex.lora_a, ex.lora_b, ex.y_in, inp.topk_ids, inp.token_lora_mapping,
+                              inp.lora_ids, add_inputs=add_inputs, adapter_enabled=adapter_enabled,
+                              topk_weights=ex.topk_weights, x_per_pair=ex.x_per_pair, y_offset=ex.y_offset,
+                              pairs=sel)
+        return {name: check_close(got[sel][:, lo:hi], ref[:, lo:hi],
+                                  "%s %s pairs %d..%d" % (w.name, name, int(sel[0]), int(sel[-1])))
+                for name, got in outs.items()}
+
+    worst = {name: 0.0 for name in outs}
+    with ThreadPoolExecutor(max_workers=max(1, host_threads())) as pool:
+        for res in pool.map(work, chunks):
+            for name, e in res.items():
+                worst[name] = max(worst[name], e)
+    return worst

@@ -86,7 +86,9 @@ def test_json_line_carries_the_contract_keys(monkeypatch, capsys, tiny):
                     align_us=0.5, counts=counts, NB=8, l2=126 << 20, footprint=400 << 20,
                     kernel_name="fused_cuda_core_kernel", align_launches=1,
                     e2e={"value": 3.0, "unit": "us/call", "h2d_bytes_per_step": 10, "d2h_bytes_per_step": 20},
-                    achieved=100.0, peak=6794.8, peak_kind="measured", inp=tiny, ex=None)
+                    achieved=100.0, peak=6794.8, peak_kind="measured", tc_peak=1895.3, tc_kind="measured",
+                    regions=[2.2, 2.0, 1.9, 2.0, 2.1], inp=tiny, ex=None,
+                    configs={"tiny": {"fused_us": 1.5, "align_us": 0.5, "step_us": 2.0}})
 
     monkeypatch.setattr(bench, "run_ours", fake_run)
     monkeypatch.setattr(bench, "time_oracle", lambda inp, b, n, ex=None, with_align=True: (5.0, "s1", 1))
@@ -109,6 +111,26 @@ def test_json_line_carries_the_contract_keys(monkeypatch, capsys, tiny):
     assert d["cpu_baseline"] == {"value": 5.0, "unit": "us/call", "cores": 1, "kind": "oracle", "sample": "s1"}
     assert d["cpu_baseline_threads"]["cores"] == 4 and d["cpu_baseline_threads"]["value"] == 2.0
     assert d["gpu_launches"] == 4 * 2
+    assert d["timed_regions"]["count"] == 5 and d["timed_regions"]["ms_median"] == 2.0
+    assert d["configs"]["tiny"]["fused_us"] == 1.5
+
+
+def test_default_workload_and_config_list():
+    """The headline is the largest configuration; the per-config entries cover
+    every configuration of the specification."""
+    import sys
+    assert bench.DEFAULT_WORKLOAD == "large_e_nact8"
+    assert bench.CONFIG_WORKLOADS == ["tiny", "decode_qwen3_w13", "decode_gptoss_w2", "prefill_mixtral_w13",
+                                      "large_e_nact1", "large_e_nact4", "large_e_nact8"]
+    for name in bench.CONFIG_WORKLOADS:
+        assert name in gen.WORKLOADS
+    old = sys.argv
+    try:
+        sys.argv = ["bench.py"]
+        a = bench.parse()
+    finally:
+        sys.argv = old
+    assert a.workload == "large_e_nact8" and a.configs == "all" and a.min_regions >= 5
 
 
 @pytest.mark.parametrize("v,name", [(0, None), (1, "smem (forced)"), (2, "global (forced)")])
@@ -127,7 +149,8 @@ def test_a_failing_threaded_baseline_does_not_lose_the_line(monkeypatch, capsys,
     def fake_run(args, world, rank, local, pg):
         return dict(ms=2.0, clocks={}, fused_us=1.5, align_us=0.5, counts=counts, NB=8, l2=1, footprint=1,
                     kernel_name="fused_cuda_core_kernel", align_launches=1, e2e=None, achieved=1.0, peak=2.0,
-                    peak_kind="measured", inp=tiny, ex=None)
+                    peak_kind="measured", tc_peak=3.0, tc_kind="measured", regions=[2.0] * 5, inp=tiny, ex=None,
+                    configs={})
 
     def boom(*a, **k):
         raise RuntimeError("threaded oracle run differs from the single-threaded one")

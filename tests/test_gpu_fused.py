@@ -165,49 +165,52 @@ def test_fused_after_either_align_variant(variant):
 
 # ---------------------------------------------------------------- full size
 
-def sampled_compare(inp, path, add_inputs=True, n_pairs=48, n_cols=48, seed=0):
-    """Full-size run; compare sampled covered pairs at sampled columns (and the
-    first / last columns of the N range) with the oracle evaluated one by one;
-    every uncovered pair must be untouched."""
+def full_size_outputs(inp, paths, add_inputs=True):
+    """Run align + fused at full size once per path; return host copies of y
+    ([M*topk, N] uint16) keyed by path."""
     import torch
-    from helpers import DeviceInputs, gpu_step, check_close, covered
+    from helpers import DeviceInputs, gpu_step, host_bf16_bits
     w = inp.w
     d = DeviceInputs(inp)
-    y, err = gpu_step(d, add_inputs=add_inputs, path=path)
-    assert err == 0, err
-    cov = covered(inp).reshape(-1)
-    rng = np.random.default_rng(seed)
-    cov_idx = np.flatnonzero(cov)
-    pairs = np.sort(rng.choice(cov_idx, min(n_pairs, len(cov_idx)), replace=False)).astype(np.int32)
-    cols = np.unique(np.concatenate([[0, w.N - 1], rng.choice(w.N, n_cols, replace=False)])).astype(np.int32)
-    ref = oracle.fused_sampled(inp.x, inp.lora_a, inp.lora_b, inp.y_in, inp.topk_ids, inp.token_lora_mapping,
-                               inp.lora_ids, pairs, cols, add_inputs=add_inputs)
-    yv = y.view(-1, w.N)
-    got = yv[torch.from_numpy(pairs.astype(np.int64)).cuda()][:, torch.from_numpy(cols.astype(np.int64)).cuda()]
-    got_bits = got.view(torch.int16).cpu().numpy().view(np.uint16)
-    check_close(got_bits, ref, w.name)
-    # every output element finite, uncovered rows bit-identical
-    assert torch.isfinite(y.float()).all()
-    unc = torch.from_numpy(np.flatnonzero(~cov).astype(np.int64)).cuda()
-    y_in = d.y_in.view(-1, w.N)
-    assert torch.equal(yv[unc].view(torch.int16), y_in[unc].view(torch.int16))
-    del d, y
+    outs = {}
+    for path in paths:
+        y, err = gpu_step(d, add_inputs=add_inputs, path=path)
+        assert err == 0, (path, err)
+        outs["path%d" % path] = host_bf16_bits(y).reshape(w.M * w.topk, w.N)
+        del y
+    del d
+    torch.cuda.empty_cache()
+    return outs
 
 
 @pytest.mark.parametrize("name", ["prefill_mixtral_w13", "large_e_nact1", "large_e_nact4", "large_e_nact8"])
-def test_fused_full_size_sampled(name):
+def test_fused_full_size_every_element(name):
+    """Full-size workloads on the kernel AUTO picks (the tensor-core kernel:
+    the persistent work split, its rings and its straddled units only occur
+    at these sizes), every covered pair and every column against the oracle.
+    On the prefill shape the CUDA-core cluster kernel runs too."""
+    from helpers import as_ex, compare_every_pair
     inp = gen.make_inputs(gen.WORKLOADS[name])
-    sampled_compare(inp, B.PATH_AUTO)
+    w = inp.w
+    assert B.fused_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size, 1,
+                                B.PATH_AUTO) == B.PATH_TCGEN05
+    paths = [B.PATH_AUTO] + ([B.PATH_CUDA_CORE_CLUSTER] if name.startswith("prefill") else [])
+    outs = full_size_outputs(inp, paths)
+    compare_every_pair(as_ex(inp), outs)
 
 
-def test_fused_prefill_full_size_cuda_core_sampled():
-    """The CUDA-core cluster kernel on the prefill shape (it is not the path AUTO
-    picks there, but it must be correct on it)."""
-    inp = gen.make_inputs(gen.WORKLOADS["prefill_mixtral_w13"])
-    sampled_compare(inp, B.PATH_CUDA_CORE_CLUSTER, add_inputs=False, n_pairs=24)
-
-
-def test_fused_prefill_full_size_stream_cc_sampled():
-    """The streaming CUDA-core kernel on the prefill shape (block 64 x rank 16)."""
-    inp = gen.make_inputs(gen.WORKLOADS["prefill_mixtral_w13"])
-    sampled_compare(inp, B.PATH_CUDA_CORE_STREAM, add_inputs=True, n_pairs=24)
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("N,rank", [(28672, 64), (14336, 128)])
+def test_fused_long_rows_small_batch_auto(M, N, rank):
+    """Small batches whose adapter rows are too long for the cluster kernel's
+    shared memory (one Mixtral-sized w13 token at rank 64 or 128): AUTO sends
+    them to the tensor-core kernel.  Every element against the oracle."""
+    from helpers import as_ex, compare_every_pair
+    w = gen.Workload("long_rows_m%d_n%d_r%d" % (M, N, rank), M=M, K=4096, N=N, E=8, topk=2, max_loras=2,
+                     num_active_loras=2, rank=rank, block_size=16, mapping="uniform", experts="uniform", seed=21)
+    assert B.fused_resolve_path(M, w.topk, w.E, w.K, N, rank, w.num_active_loras, w.block_size, 1,
+                                B.PATH_AUTO) == B.PATH_TCGEN05
+    inp = gen.make_inputs(w)
+    for add in (True, False):
+        outs = full_size_outputs(inp, [B.PATH_AUTO], add_inputs=add)
+        compare_every_pair(as_ex(inp), outs, add_inputs=add)

@@ -138,11 +138,6 @@ def test_fused_ex_one_slice_equals_plain_call():
     assert torch.equal(y.view(torch.int16), y_plain.view(torch.int16))
 
 
-def _sample_pairs(w, n, seed):
-    rng = np.random.default_rng(seed)
-    return np.sort(rng.choice(w.M * w.topk, min(n, w.M * w.topk), replace=False)).astype(np.int32)
-
-
 def test_fused_ex_gptoss_w2_full():
     """The w2 stage as the model runs it: one input row per pair and router
     weights, at the gpt-oss decode size, every pair compared."""
@@ -150,9 +145,29 @@ def test_fused_ex_gptoss_w2_full():
     run_ex(make_ex(w, x_per_pair=True, routed_weights=True), B.PATH_AUTO)
 
 
-@pytest.mark.slow
-def test_fused_ex_prefill_w13_two_slices_sampled():
+def test_fused_ex_prefill_w13_two_slices_every_element():
     """w13 with separate gate and up adapters at the Mixtral prefill size
-    (output rows 2 x 28672 wide), 64 sampled pairs compared in full."""
+    (output rows 2 x 28672 wide), every covered pair and column against the
+    oracle."""
+    import torch
+    from helpers import compare_every_pair, dev_bf16, dev_i32, host_bf16_bits
     w = gen.WORKLOADS["prefill_mixtral_w13"]
-    run_ex(make_ex(w, num_slices=2), B.PATH_AUTO, pairs=_sample_pairs(w, 64, 1))
+    ex = make_ex(w, num_slices=2)
+    inp = ex.base
+    buf = B.AlignBuffers(w.M, w.topk, w.E, w.max_loras, w.num_active_loras, w.block_size)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lora_ids = dev_i32(inp.lora_ids)
+    B.moe_lora_align(dev_i32(inp.topk_ids), dev_i32(inp.token_lora_mapping), lora_ids, w.E, w.max_loras,
+                     w.block_size, buf.sorted_token_ids, buf.expert_ids, buf.num_tokens_post_padded,
+                     workspace=buf.workspace, err_flag=err)
+    y = dev_bf16(ex.y_in)
+    B.moe_lora_fused_shrink_expand_ex(
+        dev_bf16(ex.x), [dev_bf16(a) for a in ex.lora_a], [dev_bf16(b) for b in ex.lora_b], y,
+        buf.sorted_token_ids, buf.expert_ids, buf.num_tokens_post_padded, lora_ids, w.topk, w.block_size,
+        add_inputs=True, path=B.PATH_AUTO, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = host_bf16_bits(y).reshape(w.M * w.topk, -1)
+    del y, buf
+    torch.cuda.empty_cache()
+    compare_every_pair(ex, {"auto": got})

@@ -102,6 +102,26 @@ def test_align_argument_errors():
     assert _align() == 1                          # NULL buffers
 
 
+def test_static_workspace_checks_arguments_before_size():
+    """moe_lora_align_static_workspace reports moe_lora_align's argument errors
+    first, then MOE_LORA_ERR_WORKSPACE for problems beyond its built-in buffer,
+    both before touching a device (the dummy pointers are never read)."""
+    lib = B.lib()
+    fn = lib.moe_lora_align_static_workspace
+    M, topk, E, bs = 65536, 8, 1024, 16          # workspace far beyond 4 MiB
+    cap, capb = B.max_num_tokens_padded(M, topk, E, bs), B.max_num_m_blocks(M, topk, E, bs)
+    d = ctypes.c_void_p(16)
+    # more active slots than max_loras: an argument error, not a size error
+    assert fn(d, d, d, None, M, topk, E, 8, 9, bs, d, d, d, cap, capb, None, None) == 1
+    # capacity smaller than required
+    assert fn(d, d, d, None, M, topk, E, 8, 8, bs, d, d, d, cap - 1, capb, None, None) == 1
+    # NULL outputs
+    assert fn(d, d, d, None, M, topk, E, 8, 8, bs, None, d, d, cap, capb, None, None) == 1
+    # valid arguments, workspace beyond the built-in buffer
+    assert B.align_workspace_bytes(M, topk, E, 8, bs, B.ALIGN_GLOBAL) > 4 << 20
+    assert fn(d, d, d, None, M, topk, E, 8, 8, bs, d, d, d, cap, capb, None, None) == 4
+
+
 def test_fused_argument_errors():
     assert _fused(r=132) == 2                     # rank > 128
     assert _fused(r=6) == 2                       # rank % 4 != 0
