@@ -465,8 +465,8 @@ class Rig:
             B.moe_lora_fused_shrink_expand_naive(
                 s["x"], [s["a%d" % i] for i in range(S)], [s["b%d" % i] for i in range(S)],
                 s["y"], s["topk_ids"], s["mapping"], s["lora_ids"], w.max_loras, add_inputs=True,
-                topk_weights=s.get("w"), x_per_pair=ex.x_per_pair, y_offset=ex.y_offset, err_flag=self.err,
-                stream=self.stream)
+                topk_weights=s.get("w"), x_per_pair=ex.x_per_pair, y_offset=ex.y_offset, path=args.path,
+                err_flag=self.err, stream=self.stream)
         elif ex is None:
             B.moe_lora_fused_shrink_expand(s["x"], s["a0"], s["b0"], s["y"], b.sorted_token_ids, b.expert_ids,
                                            b.num_tokens_post_padded, s["lora_ids"], w.topk, w.block_size,
@@ -532,9 +532,10 @@ def kernel_name_of(B, w, args):
     kernel = B.fused_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size,
                                   args.slices, args.path)
     name = {B.PATH_TCGEN05: "fused_tcgen05_kernel", B.PATH_CUDA_CORE_CLUSTER: "fused_cuda_core_kernel",
-            B.PATH_CUDA_CORE_STREAM: "fused_stream_cc_kernel"}[kernel]
+            B.PATH_CUDA_CORE_STREAM: "fused_cluster_stream_kernel"}[kernel]
     if args.naive:
-        name = "fused_cuda_core_kernel (naive block assignment)"
+        name = ("fused_cluster_stream_kernel" if args.path == B.PATH_CUDA_CORE_STREAM else "fused_cuda_core_kernel") \
+            + " (naive block assignment)"
     return name
 
 

@@ -85,8 +85,11 @@ typedef enum {
 #define MOE_LORA_PATH_TCGEN05 2   /* prefill-sized blocks: tcgen05 tensor-core MMAs */
 #define MOE_LORA_PATH_CUDA_CORE_CLUSTER 3 /* CUDA cores: a thread-block cluster per block, K split over
                                              its CTAs, partial t summed through distributed shared memory */
-#define MOE_LORA_PATH_CUDA_CORE_STREAM 4  /* CUDA cores: persistent CTAs stream balanced tile ranges
-                                             (rank % 8 == 0, block_size * rank <= 2048) */
+#define MOE_LORA_PATH_CUDA_CORE_STREAM 4  /* CUDA cores: persistent thread-block clusters stream each
+                                             block's adapters through a ring of TMA stages, K split over
+                                             the cluster's CTAs for the shrink (partial t pushed through
+                                             distributed shared memory), N split for the expand
+                                             (rank 8, 16, 32, 64 or 128) */
 
 /* Capacity of one LoRA row of sorted_token_ids: every pair once plus up to
  * block_size-1 padding slots for each expert: M*topk + num_experts*(block_size-1).
@@ -197,15 +200,20 @@ int moe_align_block_size(const int32_t *topk_ids, int M, int topk, int num_exper
  * rank % 8 == 0); K % 8 == 0 and N % 8 == 0; x, lora_a, lora_b, y 16-byte
  * aligned; other limits as for moe_lora_align.  The tensor-core and
  * streaming paths also need num_active_loras <= 128.
- * path: MOE_LORA_PATH_*.  AUTO picks the tensor-core path (when it takes the
- * sizes) for batches of at least 1024 pairs or when the adapters the call may
- * touch (block bound times (K + N) * rank * 2 bytes) exceed 48 MB, and the
- * cluster kernel otherwise --
- * unless the cluster kernel cannot hold a CTA's share of the adapter rows in
- * shared memory (long N * rank or K * rank rows), in which case it also picks
- * the tensor-core path when K >= 64 and N >= 32.  Shapes neither kernel
- * takes return MOE_LORA_ERR_UNSUPPORTED.  MOE_LORA_PATH_CUDA_CORE runs the
- * cluster kernel (MOE_LORA_PATH_CUDA_CORE_CLUSTER).
+ * path: MOE_LORA_PATH_*.  AUTO picks
+ *   - the tensor-core path (when it takes the sizes) for batches of at least
+ *     1024 pairs;
+ *   - for smaller batches whose adapters, by the block bound (block bound
+ *     times (K + N) * rank * 2 bytes per slice), exceed 48 MB: the cluster
+ *     streaming kernel (MOE_LORA_PATH_CUDA_CORE_STREAM) for ranks 8, 16, 32,
+ *     64 and 128, else the tensor-core path;
+ *   - otherwise the one-cluster-per-block kernel
+ *     (MOE_LORA_PATH_CUDA_CORE_CLUSTER) -- unless it cannot hold a CTA's
+ *     share of the adapter rows in shared memory (long N * rank or K * rank
+ *     rows), in which case the tensor-core path when K >= 64 and N >= 32, else
+ *     the streaming kernel.
+ * Shapes no kernel takes return MOE_LORA_ERR_UNSUPPORTED.
+ * MOE_LORA_PATH_CUDA_CORE runs MOE_LORA_PATH_CUDA_CORE_CLUSTER.
  */
 int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a,
                                  const moe_lora_bf16 *lora_b, moe_lora_bf16 *y,
@@ -278,9 +286,16 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair,
  * reported as MOE_LORA_DEVERR_EXPERT_ID, a lora_ids entry outside
  * [0, max_loras) as MOE_LORA_DEVERR_LORA_ID.  Pairs that share an adapter
  * each read it (from L2 after the first), so this path suits batches with
- * few pairs per (LoRA, expert), i.e. decode.  Runs on CUDA cores (the
- * cluster kernel); shapes whose adapter rows that kernel cannot hold in
- * shared memory return MOE_LORA_ERR_UNSUPPORTED.
+ * few pairs per (LoRA, expert), i.e. decode.  Runs on CUDA cores:
+ *   path  MOE_LORA_PATH_CUDA_CORE_CLUSTER or MOE_LORA_PATH_CUDA_CORE (one
+ *         cluster per pair, the whole share of A and B in shared memory;
+ *         shapes whose rows it cannot hold return MOE_LORA_ERR_UNSUPPORTED),
+ *         MOE_LORA_PATH_CUDA_CORE_STREAM (persistent CTAs streaming each
+ *         pair's adapters; rank 8, 16, 32, 64 or 128), or MOE_LORA_PATH_AUTO:
+ *         the streaming kernel when the pairs' adapters (M * topk * slices *
+ *         (K + N) * rank * 2 bytes) exceed 48 MB and it takes the rank, else
+ *         the one-cluster-per-pair kernel.  MOE_LORA_PATH_TCGEN05 is not
+ *         valid here.
  *
  *   topk_ids          [device] int32 [M, topk]
  *   token_lora_mapping [device] int32 [M] (-1: no adapter)
@@ -294,8 +309,8 @@ int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair,
                                        const int32_t *token_lora_mapping, const int32_t *lora_ids,
                                        const int32_t *adapter_enabled, int M, int topk,
                                        int num_experts, int K, int N, int rank, int max_loras,
-                                       int num_active_loras, int add_inputs, int32_t *err_flag,
-                                       void *stream);
+                                       int num_active_loras, int add_inputs, int path,
+                                       int32_t *err_flag, void *stream);
 
 /*
  * moe_lora_fused_resolve_path -- the kernel a fused call with these sizes

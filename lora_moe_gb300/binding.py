@@ -70,7 +70,8 @@ def lib() -> ctypes.CDLL:
             L.moe_align_block_size.argtypes = [P, I, I, I, I, P, P, P, I, I, P, S, I, P, P]
             L.moe_lora_fused_shrink_expand_naive.restype = I
             L.moe_lora_fused_shrink_expand_naive.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P), I, P, I, I,
-                                                             P, P, P, P, P, I, I, I, I, I, I, I, I, I, P, P]
+                                                             P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P,
+                                                             P]
             L.moe_lora_fused_plan.restype = I
             L.moe_lora_fused_plan.argtypes = [I] * 12 + [P]
             L.moe_lora_fused_resolve_path.restype = I
@@ -266,10 +267,11 @@ def moe_lora_fused_shrink_expand_ex(x, lora_a, lora_b, y, sorted_token_ids, expe
 
 def moe_lora_fused_shrink_expand_naive(x, lora_a, lora_b, y, topk_ids, token_lora_mapping, lora_ids, max_loras,
                                        add_inputs=True, adapter_enabled=None, topk_weights=None, x_per_pair=False,
-                                       y_offset=0, err_flag=None, stream=None):
+                                       y_offset=0, path=PATH_AUTO, err_flag=None, stream=None):
     """moe_lora_fused_shrink_expand_naive (no align: one work item per pair) on
     device tensors; y [M, topk, ldy] is updated in place.  lora_a / lora_b: a
-    tensor or a list of per-slice tensors."""
+    tensor or a list of per-slice tensors.  path: PATH_AUTO, PATH_CUDA_CORE,
+    PATH_CUDA_CORE_CLUSTER or PATH_CUDA_CORE_STREAM."""
     if isinstance(lora_a, torch.Tensor):
         lora_a, lora_b = [lora_a], [lora_b]
     S = len(lora_a)
@@ -297,7 +299,7 @@ def moe_lora_fused_shrink_expand_naive(x, lora_a, lora_b, y, topk_ids, token_lor
         _ptr(topk_weights, torch.float32, "topk_weights"), _ptr(topk_ids, torch.int32, "topk_ids"),
         _ptr(token_lora_mapping, torch.int32, "token_lora_mapping"), _ptr(lora_ids, torch.int32, "lora_ids"),
         _ptr(adapter_enabled, torch.int32, "adapter_enabled"), M, topk, E, K, N, r, L, lora_ids.numel(),
-        int(bool(add_inputs)), _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+        int(bool(add_inputs)), int(path), _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
     _check(st, "moe_lora_fused_shrink_expand_naive")
 
 

@@ -16,7 +16,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libmoe_lora.so")
 SOURCES = ["api.cu", "align.cu", "fused_cuda_core.cu", "fused_tcgen05.cu", "stream_pipeline.cu",
-           "fused_stream_cc.cu", "align_static_workspace.cu"]
+           "fused_stream_cluster.cu", "align_static_workspace.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

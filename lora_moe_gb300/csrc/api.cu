@@ -47,6 +47,14 @@ constexpr int kMaxSlots = 512;
 
 bool valid_block_size(int bs) { return bs == 16 || bs == 32 || bs == 64 || bs == 128; }
 
+// Ranks each forced path takes: the tensor-core kernel rank % 8 == 0, the
+// cluster streaming kernel the powers of two 8 .. 128.
+bool path_takes_rank(int path, int rank) {
+  if (path == MOE_LORA_PATH_TCGEN05) return rank % 8 == 0;
+  if (path == MOE_LORA_PATH_CUDA_CORE_STREAM) return rank >= 8 && rank <= 128 && (rank & (rank - 1)) == 0;
+  return true;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 long long capacity_tokens(int M, int topk, int E, int bs) {
@@ -191,30 +199,59 @@ static bool cluster_kernel_fits(const FusedArgs &f, size_t max_smem) {
   return plan_fused_cuda_core(f, dev, &plan) == 0;
 }
 
-// The kernel a fused call runs.  AUTO takes the tensor-core kernel (when it
-// supports the sizes) for batches of at least 1024 pairs or when the adapter
-// bytes the call may touch, by the block bound, exceed 48 MB: there the
-// balanced persistent tile ranges keep every SM streaming.  Otherwise, and for
-// MOE_LORA_PATH_CUDA_CORE, the cluster kernel: on every decode workload
-// measured it beat the streaming CUDA-core kernel, which recomputes the shrink
-// of a block in every CTA whose tile range touches it.  Small batches whose
-// adapter rows are too long for the cluster kernel's shared memory (N * rank
-// or K * rank beyond what 16 CTAs hold) also go to the tensor-core kernel when
-// K and N span at least one 64-wide K tile and 32 output columns.
+// The kernel a fused call runs.
+//   * Batches of at least 1024 pairs: the tensor-core kernel (when it supports
+//     the sizes): blocks hold enough pairs for a real contraction.
+//   * Smaller (decode) batches whose adapters, by the block bound, exceed
+//     48 MB: the cluster streaming kernel (when it takes the rank), which
+//     splits each block over a 4-CTA cluster and keeps every SM streaming
+//     (gpt-oss-shaped w2 decode: 64 us, against 93 us on tensor cores).
+//   * Other decode batches, and MOE_LORA_PATH_CUDA_CORE: the one-cluster-per-
+//     block kernel (Qwen3-shaped w13 decode: 7.9 us, against 11.1 us
+//     streaming) -- unless its shared memory cannot hold a CTA's share of the
+//     adapter rows (N * rank or K * rank beyond what 16 CTAs hold): then the
+//     tensor-core kernel when K and N span at least one 64-wide K tile and 32
+//     output columns, else the streaming kernel.
 static int resolve_path(const FusedArgs &f, int path, size_t max_smem) {
   int use = path;
   if (use == MOE_LORA_PATH_AUTO) {
     const double touched = (double)fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size) *
                            f.num_slices * (double)(f.K + f.N) * f.rank * 2.0;
-    const bool big = (long long)f.M * f.topk >= 1024 || touched > 48.0e6;
+    const bool prefill = (long long)f.M * f.topk >= 1024;
     const bool tc = tcgen05_path_supports(f);
-    if (tc && (big || (f.K >= 64 && f.N >= 32 && !cluster_kernel_fits(f, max_smem))))
+    const bool stream = cluster_stream_supports(f);
+    if (prefill && tc)
       use = MOE_LORA_PATH_TCGEN05;
+    else if (!prefill && touched > 48.0e6 && stream)
+      use = MOE_LORA_PATH_CUDA_CORE_STREAM;
+    else if (!prefill && touched > 48.0e6 && tc)
+      use = MOE_LORA_PATH_TCGEN05;
+    else if (cluster_kernel_fits(f, max_smem))
+      use = MOE_LORA_PATH_CUDA_CORE;
+    else if (tc && f.K >= 64 && f.N >= 32)
+      use = MOE_LORA_PATH_TCGEN05;
+    else if (stream)
+      use = MOE_LORA_PATH_CUDA_CORE_STREAM;
     else
       use = MOE_LORA_PATH_CUDA_CORE;
   }
   if (use == MOE_LORA_PATH_CUDA_CORE) use = MOE_LORA_PATH_CUDA_CORE_CLUSTER;
   return use;
+}
+
+// The kernel a naive-assignment call runs (a path value), or -status.  AUTO
+// takes the cluster streaming kernel when the pairs' adapters exceed 48 MB
+// (gpt-oss-shaped w2 decode: 51 us, against 96 us) and it takes the rank,
+// else the one-cluster-per-pair kernel (Qwen3-shaped decode: 7.6 us,
+// against 12.9 us streaming), which MOE_LORA_PATH_CUDA_CORE also names.
+static int resolve_naive_path(const FusedArgs &f, int path) {
+  const bool stream = cluster_stream_supports(f);
+  if (path == MOE_LORA_PATH_CUDA_CORE_STREAM) return stream ? MOE_LORA_PATH_CUDA_CORE_STREAM : -MOE_LORA_ERR_UNSUPPORTED;
+  if (path == MOE_LORA_PATH_AUTO && stream) {
+    const double touched = (double)f.M * f.topk * f.num_slices * (double)(f.K + f.N) * f.rank * 2.0;
+    if (touched > 48.0e6) return MOE_LORA_PATH_CUDA_CORE_STREAM;
+  }
+  return MOE_LORA_PATH_CUDA_CORE_CLUSTER;
 }
 
 namespace moe_lora {
@@ -305,8 +342,7 @@ static int resolve_path_query(int M, int topk, int num_experts, int K, int N, in
       num_slices < 1 || num_slices > kMaxSlices || path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_CUDA_CORE_STREAM)
     return -MOE_LORA_ERR_INVALID_ARG;
   if (!valid_block_size(block_size) || rank > kMaxRank || rank % 4 != 0) return -MOE_LORA_ERR_UNSUPPORTED;
-  if ((path == MOE_LORA_PATH_TCGEN05 || path == MOE_LORA_PATH_CUDA_CORE_STREAM) && rank % 8 != 0)
-    return -MOE_LORA_ERR_UNSUPPORTED;
+  if (!path_takes_rank(path, rank)) return -MOE_LORA_ERR_UNSUPPORTED;
   FusedArgs f = {};
   f.M = M;
   f.topk = topk;
@@ -333,7 +369,6 @@ int moe_lora_fused_plan(int M, int topk, int num_experts, int K, int N, int rank
   const int use = resolve_path_query(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices,
                                      path, (size_t)max_smem_per_block);
   if (use < 0) return -use;
-  if (use == MOE_LORA_PATH_CUDA_CORE_STREAM) return MOE_LORA_ERR_UNSUPPORTED;
   FusedArgs f = {};
   f.M = M;
   f.topk = topk;
@@ -351,7 +386,9 @@ int moe_lora_fused_plan(int M, int topk, int num_experts, int K, int N, int rank
   dev.minor = 3;
   dev.max_smem_optin = (size_t)max_smem_per_block;
   FusedPlan plan = {};
-  const int st = use == MOE_LORA_PATH_TCGEN05 ? plan_fused_tcgen05(f, dev, &plan) : plan_fused_cuda_core(f, dev, &plan);
+  const int st = use == MOE_LORA_PATH_TCGEN05          ? plan_fused_tcgen05(f, dev, &plan)
+                 : use == MOE_LORA_PATH_CUDA_CORE_STREAM ? plan_fused_cluster_stream(f, dev, false, &plan)
+                                                         : plan_fused_cuda_core(f, dev, &plan);
   if (st) return st;
   const int32_t vals[11] = {plan.kernel, plan.grid, plan.threads, plan.smem_bytes, plan.s_sh, plan.lag, plan.s_ex,
                             plan.t_bufs, plan.tmem_cols, plan.cluster, plan.pairs_per_group};
@@ -371,8 +408,7 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair, cons
                             max_num_m_blocks))
     return st;
   if (path < MOE_LORA_PATH_AUTO || path > MOE_LORA_PATH_CUDA_CORE_STREAM) return MOE_LORA_ERR_INVALID_ARG;
-  if ((path == MOE_LORA_PATH_TCGEN05 || path == MOE_LORA_PATH_CUDA_CORE_STREAM) && rank % 8 != 0)
-    return MOE_LORA_ERR_UNSUPPORTED;
+  if (!path_takes_rank(path, rank)) return MOE_LORA_ERR_UNSUPPORTED;
   FusedArgs f;
   bool empty = false;
   if (int st = prepare_fused(x, x_per_pair, lora_a, lora_b, num_slices, y, ldy, y_offset, topk_weights, lora_ids,
@@ -393,7 +429,7 @@ int moe_lora_fused_shrink_expand_ex(const moe_lora_bf16 *x, int x_per_pair, cons
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   switch (use) {
     case MOE_LORA_PATH_TCGEN05: return launch_fused_tcgen05(f, s);
-    case MOE_LORA_PATH_CUDA_CORE_STREAM: return launch_fused_stream_cc(f, s);
+    case MOE_LORA_PATH_CUDA_CORE_STREAM: return launch_fused_cluster_stream(f, s);
     default: return launch_fused_cuda_core(f, s);
   }
 }
@@ -404,8 +440,12 @@ int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair, c
                                        const int32_t *token_lora_mapping, const int32_t *lora_ids,
                                        const int32_t *adapter_enabled, int M, int topk, int num_experts, int K,
                                        int N, int rank, int max_loras, int num_active_loras, int add_inputs,
-                                       int32_t *err_flag, void *stream) {
+                                       int path, int32_t *err_flag, void *stream) {
   if (M < 0 || topk < 1 || num_experts < 1 || max_loras < 1 || num_active_loras < 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (path != MOE_LORA_PATH_AUTO && path != MOE_LORA_PATH_CUDA_CORE && path != MOE_LORA_PATH_CUDA_CORE_CLUSTER &&
+      path != MOE_LORA_PATH_CUDA_CORE_STREAM)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (!path_takes_rank(path, rank)) return MOE_LORA_ERR_UNSUPPORTED;
   if (num_experts > kMaxExperts || topk > num_experts) return MOE_LORA_ERR_UNSUPPORTED;
   if (num_active_loras > max_loras) return MOE_LORA_ERR_INVALID_ARG;
   if ((long long)M * topk > INT32_MAX / 2) return MOE_LORA_ERR_UNSUPPORTED;
@@ -419,6 +459,9 @@ int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair, c
   if (!topk_ids || !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
   f.topk_ids = topk_ids;
   f.token_lora_mapping = token_lora_mapping;
+  const int use = resolve_naive_path(f, path);
+  if (use < 0) return -use;
+  if (use == MOE_LORA_PATH_CUDA_CORE_STREAM) return launch_fused_cluster_stream_naive(f, static_cast<cudaStream_t>(stream));
   return launch_fused_naive(f, static_cast<cudaStream_t>(stream));
 }
 

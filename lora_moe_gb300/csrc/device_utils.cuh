@@ -83,6 +83,61 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   }
 }
 
+// Wait for the phase with the given parity, acquiring at cluster scope (for
+// phases completed by peers' remote arrivals or st.async writes).  Bounded
+// like mbar_wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                                  int32_t *err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    if (*abort) return false;
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+      *abort = 1;
+      flag_error(err, MOE_LORA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// ------------------------------------------------------ distributed shared memory
+
+// Shared::cluster address of the variable at shared::cta address `saddr` in
+// the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+
+// Arrive on the mbarrier at shared::cluster address `rbar` (a peer's, or this
+// CTA's own), releasing this thread's earlier memory operations at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
+
+// Asynchronous 16-byte store into a peer's (or this CTA's) shared memory at
+// shared::cluster address `raddr`; its bytes are counted as completed
+// transactions on the mbarrier at shared::cluster address `rbar` of the same CTA.
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   raddr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(rbar)
+               : "memory");
+}
+
 // ------------------------------------------------------------ async copies
 
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
@@ -150,6 +205,21 @@ __device__ __forceinline__ void fence_proxy_async_cluster() {
 // Named barrier over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Named barrier over `count` threads that also ANDs `pred` over them: every
+// participant gets the same answer.
+__device__ __forceinline__ bool named_barrier_and(int id, int count, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
 // Cluster barrier halves.  arrive.release orders this thread's earlier memory

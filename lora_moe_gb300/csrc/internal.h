@@ -99,9 +99,11 @@ int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream);
 // Whether the tensor-core path takes these arguments (rank % 8 == 0, at most
 // 128 listed slots).
 bool tcgen05_path_supports(const FusedArgs &f);
-// The CUDA-core streaming kernel (decode-sized blocks, large adapters).
-int launch_fused_stream_cc(const FusedArgs &f, cudaStream_t stream);
-bool stream_cc_supports(const FusedArgs &f);
+// The cluster streaming kernel (CUDA cores; decode-sized blocks): sorted and
+// naive block assignment.  Takes rank % 8 == 0, at most 128 listed slots.
+bool cluster_stream_supports(const FusedArgs &f);
+int launch_fused_cluster_stream(const FusedArgs &f, cudaStream_t stream);
+int launch_fused_cluster_stream_naive(const FusedArgs &f, cudaStream_t stream);
 
 // Device properties of the current device, cached per device.
 struct DeviceInfo {
@@ -121,5 +123,6 @@ struct FusedPlan {
 };
 int plan_fused_tcgen05(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *out);
 int plan_fused_cuda_core(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *out);
+int plan_fused_cluster_stream(const FusedArgs &f, const DeviceInfo &dev, bool naive, FusedPlan *out);
 
 }  // namespace moe_lora

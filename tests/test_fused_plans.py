@@ -19,9 +19,9 @@ def plan_of(w, **kw):
 
 # (kernel, shrink stages, lag, expand stages, T buffers, TMEM columns) for the
 # tensor-core kernel; (kernel, CTAs per cluster, pairs per group) for the
-# cluster kernel.  These are the plans the measured numbers were taken with.
+# CUDA-core kernels.  These are the plans the measured numbers were taken with.
 PINNED = {
-    "decode_gptoss_w2": (B.PATH_TCGEN05, 10, 4, 6, 1, 128),
+    "decode_gptoss_w2": (B.PATH_CUDA_CORE_STREAM, 4, 4),
     "prefill_mixtral_w13": (B.PATH_TCGEN05, 10, 4, 6, 1, 256),
     "large_e_nact1": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
     "large_e_nact8": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
@@ -45,7 +45,7 @@ SHAPES = list(itertools.product([16, 256, 4096], [2, 8], [8, 128, 256], [1024, 4
                                 [8, 16, 64, 128], [16, 64, 128]))
 
 
-@pytest.mark.parametrize("path", [B.PATH_TCGEN05, B.PATH_CUDA_CORE_CLUSTER])
+@pytest.mark.parametrize("path", [B.PATH_TCGEN05, B.PATH_CUDA_CORE_CLUSTER, B.PATH_CUDA_CORE_STREAM])
 def test_plan_invariants(path):
     checked = 0
     for M, topk, E, K, N, r, bs in SHAPES:
@@ -69,6 +69,16 @@ def test_plan_invariants(path):
             per_sm = max(1, (228 * 1024) // (p["smem_bytes"] + 1024))
             assert per_sm * p["tmem_cols"] <= 512, p                      # co-resident CTAs fit in TMEM
             assert p["threads"] == 416 and 1 <= p["grid"] <= 152 * per_sm
+        elif path == B.PATH_CUDA_CORE_STREAM:
+            # clusters of 1..8 CTAs, one per SM; each CTA holds at least one
+            # 8-wide chunk of K and of N; a ring of at least 4 stages
+            C = p["cluster"]
+            assert C in (1, 2, 4, 8) and C <= min(K // 8, N // 8), (K, N, p)
+            assert p["grid"] % C == 0 and 1 <= p["grid"] <= 2 * 152, p
+            assert p["s_sh"] >= 4 and p["threads"] == 320, p
+            assert p["smem_bytes"] <= 113 * 1024, p
+            assert p["pairs_per_group"] == 4, p
+            assert r * p["s_ex"] * 2 <= 16384 and p["t_bufs"] * r * 2 <= 16384, p   # A box, B rows per stage
         else:
             assert 1 <= p["cluster"] <= 16 and p["pairs_per_group"] in (1, 2, 8)
     assert checked > 100
@@ -118,13 +128,42 @@ def test_auto_plans_every_shape_with_a_full_k_tile():
         if topk > E:
             continue
         p = B.fused_plan(M, topk, E, K, N, r, nact, bs, **GB300)
-        assert p["kernel"] in (B.PATH_TCGEN05, B.PATH_CUDA_CORE_CLUSTER)
+        assert p["kernel"] in (B.PATH_TCGEN05, B.PATH_CUDA_CORE_CLUSTER, B.PATH_CUDA_CORE_STREAM)
+        if p["kernel"] == B.PATH_CUDA_CORE_STREAM:   # decode batches with large adapters only
+            assert M * topk < 1024 and r in (8, 16, 32, 64, 128)
+        if M * topk >= 1024:
+            assert p["kernel"] == B.PATH_TCGEN05
         n += 1
     assert n > 1000
+
+
+def test_auto_streams_large_decode_adapters():
+    """Decode batches whose adapters, by the block bound, exceed 48 MB go to
+    the cluster streaming kernel (the gpt-oss-shaped w2 decode); small
+    adapters stay on the one-cluster-per-block kernel (the Qwen3-shaped w13
+    decode); prefill-sized batches go to tensor cores."""
+    R = B.fused_resolve_path
+    assert R(64, 4, 128, 2880, 2880, 64, 6, 16) == B.PATH_CUDA_CORE_STREAM
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 16) == B.PATH_CUDA_CORE_CLUSTER
+    assert R(8192, 2, 8, 4096, 28672, 16, 4, 64) == B.PATH_TCGEN05
+    assert R(64, 4, 128, 2880, 2880, 72, 6, 16) == B.PATH_TCGEN05          # rank the streaming kernel lacks
 
 
 def test_plan_rejects_what_the_kernel_cannot_run():
     with pytest.raises(B.MoeLoraError):
         B.fused_plan(64, 4, 128, 2880, 2880, 12, 6, 16, path=B.PATH_TCGEN05, **GB300)   # rank % 8 != 0
     with pytest.raises(B.MoeLoraError):
-        B.fused_plan(64, 4, 128, 2880, 2880, 64, 6, 16, path=B.PATH_CUDA_CORE_STREAM, **GB300)
+        B.fused_plan(64, 4, 128, 2880, 2880, 12, 6, 16, path=B.PATH_CUDA_CORE_STREAM, **GB300)  # rank % 8 != 0
+
+
+def test_cluster_stream_plan_gptoss_decode():
+    """The cluster streaming kernel on the gpt-oss decode shape: clusters of
+    4 CTAs, two CTAs of 10 warps per SM, each with a ring of 17 KB stages (A
+    boxes of 64 ranks x 128 columns, B pieces of 128 rows x 64 ranks, each with
+    the pairs' x or y_in pieces)."""
+    p = B.fused_plan(64, 4, 128, 2880, 2880, 64, 6, 16, path=B.PATH_CUDA_CORE_STREAM, **GB300)
+    assert p["kernel"] == B.PATH_CUDA_CORE_STREAM
+    assert p["cluster"] in (1, 2, 4, 8) and p["grid"] % p["cluster"] == 0 and p["grid"] <= 2 * 152
+    assert p["cluster"] == 4 and p["s_sh"] == 5 and p["threads"] == 320  # cluster, ring stages, threads
+    assert p["s_ex"] == 128 and p["t_bufs"] == 128                      # A columns, B rows per stage
+    assert p["smem_bytes"] <= 113 * 1024                                # two CTAs share an SM

@@ -26,12 +26,12 @@ ALL_PATHS = [B.PATH_CUDA_CORE_CLUSTER, B.PATH_CUDA_CORE_STREAM, B.PATH_TCGEN05]
 
 
 def skip_unsupported(w, path):
-    """The streaming CUDA-core kernel and the tensor-core kernel need rank % 8 == 0;
-    the streaming kernel also block_size * rank <= 2048."""
-    if path in (B.PATH_TCGEN05, B.PATH_CUDA_CORE_STREAM) and w.rank % 8:
+    """The tensor-core kernel needs rank % 8 == 0, the cluster streaming kernel
+    a rank of 8, 16, 32, 64 or 128."""
+    if path == B.PATH_TCGEN05 and w.rank % 8:
         pytest.skip("path needs rank % 8 == 0")
-    if path == B.PATH_CUDA_CORE_STREAM and w.block_size * w.rank > 2048:
-        pytest.skip("streaming CUDA-core kernel needs block_size * rank <= 2048")
+    if path == B.PATH_CUDA_CORE_STREAM and w.rank not in (8, 16, 32, 64, 128):
+        pytest.skip("path needs a power-of-two rank of 8 .. 128")
 
 
 def run_and_compare_full(inp, path, add_inputs=True, adapter_enabled=None, variant=B.ALIGN_AUTO):
@@ -78,6 +78,15 @@ def test_fused_random_shapes(seed, path):
     run_and_compare_full(inp, path, add_inputs=bool(seed % 2))
 
 
+@pytest.mark.parametrize("seed", range(12))
+def test_fused_random_shapes_cluster_stream(seed):
+    """The cluster streaming kernel on random shapes with its ranks (8 .. 128,
+    powers of two): ragged K and N, every block size, both add modes."""
+    rank = [8, 16, 32, 64, 128][seed % 5]
+    inp = gen.make_inputs(small_workload(600 + seed, rank=rank))
+    run_and_compare_full(inp, B.PATH_CUDA_CORE_STREAM, add_inputs=bool(seed % 2))
+
+
 @pytest.mark.parametrize("rank", [4, 12, 20])
 def test_fused_small_ranks_cuda_core(rank):
     inp = gen.make_inputs(small_workload(77, rank=rank, K=136, N=264))
@@ -105,7 +114,7 @@ def test_fused_exact_integer_case(path, rank, nnz):
     the tails."""
     from helpers import DeviceInputs, gpu_step, host_bf16_bits
     w = gen.Workload("int", M=70, K=264, N=392, E=3, topk=2, max_loras=2, num_active_loras=2, rank=rank,
-                     block_size=64 if path != B.PATH_CUDA_CORE_STREAM else 16, mapping="uniform_with_none",
+                     block_size=64, mapping="uniform_with_none",
                      experts="uniform", seed=3)
     inp = gen.make_inputs(w)
     rng = np.random.default_rng(8)

@@ -104,6 +104,18 @@ def test_fused_ex_random_shapes(seed, path):
     run_ex(make_ex(w, **opt), path, add_inputs=bool(seed % 2))
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_fused_ex_random_shapes_cluster_stream(seed):
+    """The cluster streaming kernel with a random mix of the options, at its
+    ranks (powers of two, 8 .. 128)."""
+    w = small_workload(700 + seed, rank=[8, 16, 32, 64, 128][seed % 5])
+    rng = np.random.default_rng(seed)
+    opt = dict(num_slices=int(rng.integers(1, 5)), x_per_pair=bool(rng.integers(0, 2)),
+               routed_weights=bool(rng.integers(0, 2)), y_offset=8 * int(rng.integers(0, 3)),
+               extra=8 * int(rng.integers(0, 3)))
+    run_ex(make_ex(w, **opt), B.PATH_CUDA_CORE_STREAM, add_inputs=bool(seed % 2))
+
+
 @pytest.mark.parametrize("rank", [4, 12])
 def test_fused_ex_small_ranks_cuda_core(rank):
     w = small_workload(77, rank=rank, K=136, N=264)

@@ -180,14 +180,17 @@ def test_fused_resolve_path():
     # decode-sized, small adapters -> cluster kernel; many pairs -> tensor cores
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 0) == 3
     assert R(8192, 2, 8, 4096, 28672, 16, 4, 64, 1, 0) == 2
-    # few pairs but large adapters (block bound x (K + N) x r x 2 bytes > 48 MB) -> tensor cores
-    assert R(64, 4, 128, 2880, 2880, 64, 6, 16, 1, 0) == 2
+    # few pairs but large adapters (block bound x (K + N) x r x 2 bytes > 48 MB) -> cluster
+    # streaming kernel, or tensor cores for a rank it does not take
+    assert R(64, 4, 128, 2880, 2880, 64, 6, 16, 1, 0) == 4
+    assert R(64, 4, 128, 2880, 2880, 72, 6, 16, 1, 0) == 2
     # rank % 8 != 0 keeps the CUDA cores
     assert R(8192, 2, 8, 4096, 28672, 12, 4, 64, 1, 0) == 3
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 1) == 3   # CUDA_CORE -> cluster
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 4) == 4
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 2) == 2
     assert R(16, 8, 128, 2048, 1536, 12, 2, 16, 1, 2) == -2  # tensor cores need rank % 8 == 0
+    assert R(16, 8, 128, 2048, 1536, 24, 2, 16, 1, 4) == -2  # streaming: ranks 8, 16, 32, 64, 128
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 5, 0) == -1  # too many slices
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 9) == -1
 
@@ -209,7 +212,7 @@ def test_fused_naive_argument_errors():
     def naive(slices=1, **kw):
         args = dict(x=None, x_per_pair=0, a=(P * max(slices, 1))(), b=(P * max(slices, 1))(), S=slices, y=None,
                     ldy=512, y_off=0, w=None, topk_ids=None, mapping=None, lora_ids=None, enabled=None, M=16,
-                    topk=2, E=8, K=256, N=512, r=8, L=2, nact=2, add=1, err=None, stream=None)
+                    topk=2, E=8, K=256, N=512, r=8, L=2, nact=2, add=1, path=0, err=None, stream=None)
         args.update(kw)
         return B.lib().moe_lora_fused_shrink_expand_naive(*args.values())
 
@@ -222,6 +225,10 @@ def test_fused_naive_argument_errors():
     assert naive(nact=0) == 0          # zero grid
     assert naive(M=0) == 0
     assert naive() == 1                # NULL buffers
+    assert naive(path=2) == 1          # the tensor-core kernel has no naive assignment
+    assert naive(path=9) == 1
+    assert naive(path=4, r=12) == 2    # the cluster streaming kernel takes ranks 8, 16, 32, 64, 128
+    assert naive(path=4, r=24) == 2
 
 
 def test_plain_c_consumer(tmp_path):
@@ -265,7 +272,8 @@ int main(void) {
                                         8, 256, 512, 8, 2, 2, 16, 152, 10, 1, MOE_LORA_PATH_AUTO, NULL, NULL)
         != MOE_LORA_ERR_INVALID_ARG) return 12;
     if (moe_lora_fused_shrink_expand_naive(NULL, 0, a, b, 1, NULL, 512, 0, NULL, NULL, NULL, NULL, NULL, 16, 2, 8,
-                                           260, 512, 8, 2, 2, 1, NULL, NULL) != MOE_LORA_ERR_MISALIGNED) return 13;
+                                           260, 512, 8, 2, 2, 1, MOE_LORA_PATH_AUTO, NULL, NULL)
+        != MOE_LORA_ERR_MISALIGNED) return 13;
     if (moe_lora_align_workspace_bytes(4096, 8, 256, 1, 64, MOE_LORA_ALIGN_GLOBAL) == 0) return 14;
   }
   printf("ok\n");
