@@ -78,6 +78,8 @@ typedef enum {
 #define MOE_LORA_ALIGN_AUTO 0
 #define MOE_LORA_ALIGN_SMEM 1     /* one CTA per active slot, counters in shared memory */
 #define MOE_LORA_ALIGN_GLOBAL 2   /* many CTAs per slot, counters in the caller's workspace */
+#define MOE_LORA_ALIGN_CLUSTER 3  /* a thread-block cluster of up to 8 CTAs per slot in one launch,
+                                     counts exchanged through distributed shared memory (no workspace) */
 
 /* Fused paths (moe_lora_fused_shrink_expand `path`). */
 #define MOE_LORA_PATH_AUTO 0
@@ -100,9 +102,17 @@ int moe_lora_max_num_tokens_padded(int M, int topk, int num_experts, int block_s
  * Returns -1 on invalid sizes. */
 int moe_lora_max_num_m_blocks(int M, int topk, int num_experts, int block_size);
 
+/* The align variant a call with these sizes runs: MOE_LORA_ALIGN_SMEM,
+ * MOE_LORA_ALIGN_GLOBAL or MOE_LORA_ALIGN_CLUSTER (never AUTO), or a negative
+ * moe_lora_status code for invalid sizes or a variant these sizes do not fit.
+ * Host only; no device is touched. */
+int moe_lora_align_resolve_variant(int M, int topk, int num_experts, int variant);
+
 /* Bytes of [device] workspace moe_lora_align needs for `variant` (0 for the
- * shared-memory variant; for AUTO, the size of whichever variant AUTO picks for
- * these sizes).  Returns 0 and the call needs no workspace when it is 0. */
+ * shared-memory and cluster variants; for AUTO, the size of whichever variant
+ * AUTO picks for these sizes).  Returns 0 and the call needs no workspace
+ * when it is 0.  AUTO picks the cluster variant for num_experts >= 256 or at
+ * least 16384 pairs, and the shared-memory variant otherwise. */
 size_t moe_lora_align_workspace_bytes(int M, int topk, int num_experts,
                                       int num_active_loras, int block_size, int variant);
 

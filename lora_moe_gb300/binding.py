@@ -17,7 +17,7 @@ import torch
 from . import build as _build
 
 MOE_LORA_OK = 0
-ALIGN_AUTO, ALIGN_SMEM, ALIGN_GLOBAL = 0, 1, 2
+ALIGN_AUTO, ALIGN_SMEM, ALIGN_GLOBAL, ALIGN_CLUSTER = 0, 1, 2, 3
 PATH_AUTO, PATH_CUDA_CORE, PATH_TCGEN05, PATH_CUDA_CORE_CLUSTER, PATH_CUDA_CORE_STREAM = 0, 1, 2, 3, 4
 DEVERR_EXPERT_ID, DEVERR_LORA_ID, DEVERR_CAPACITY, DEVERR_PAIR_ID, DEVERR_TIMEOUT = 1, 2, 4, 8, 16
 
@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_max_num_tokens_padded.argtypes = [I, I, I, I]
             L.moe_lora_max_num_m_blocks.restype = I
             L.moe_lora_max_num_m_blocks.argtypes = [I, I, I, I]
+            L.moe_lora_align_resolve_variant.restype = I
+            L.moe_lora_align_resolve_variant.argtypes = [I, I, I, I]
             L.moe_lora_align_workspace_bytes.restype = S
             L.moe_lora_align_workspace_bytes.argtypes = [I, I, I, I, I, I]
             L.moe_lora_align.restype = I
@@ -90,6 +92,15 @@ def max_num_tokens_padded(M: int, topk: int, num_experts: int, block_size: int) 
 
 def max_num_m_blocks(M: int, topk: int, num_experts: int, block_size: int) -> int:
     return lib().moe_lora_max_num_m_blocks(M, topk, num_experts, block_size)
+
+
+def align_resolve_variant(M, topk, num_experts, variant=ALIGN_AUTO) -> int:
+    """The align variant a call with these sizes runs (ALIGN_SMEM, ALIGN_GLOBAL
+    or ALIGN_CLUSTER)."""
+    v = lib().moe_lora_align_resolve_variant(M, topk, num_experts, variant)
+    if v < 0:
+        raise MoeLoraError(-v, "moe_lora_align_resolve_variant")
+    return v
 
 
 def align_workspace_bytes(M, topk, num_experts, num_active_loras, block_size, variant=ALIGN_AUTO) -> int:

@@ -21,12 +21,15 @@
 //   global-memory variant : many CTAs per slot; per-warp counters go to the
 //                           caller's workspace and three launches (count, scan,
 //                           scatter) replace the CTA-wide barriers.
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 
 #include "device_utils.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace moe_lora {
 
@@ -163,17 +166,45 @@ __device__ bool write_segments(const AlignArgs &a, int l, const int *cnt, int *o
 
 constexpr int kCache = 8;   // warp-widths of expert ids a lane keeps between the two walks
 
-// The two walks of one warp over [lo, hi) with the experts kept in registers
-// between them (hi - lo <= kCache * 32); `tab` is this warp's counter row.
+// The routing of a warp's pairs [lo, hi) (hi - lo <= kCache * 32), loaded
+// into registers in one round trip, before the slot's LoRA index is known:
+// rm[it] the LoRA of pair lo + 32 it + lane's token (kNoSlot past hi; the
+// slot itself, 0, without a mapping), re[it] its expert id.
+constexpr int kNoSlot = -2;
+__device__ __forceinline__ void warp_load_routing(const AlignArgs &a, int lo, int hi, int lane, int (&rm)[kCache],
+                                                  int (&re)[kCache]) {
+#pragma unroll
+  for (int it = 0; it < kCache; ++it) {
+    const int f = lo + it * 32 + lane;
+    rm[it] = kNoSlot;
+    re[it] = -1;
+    if (f < hi) {
+      rm[it] = a.token_lora_mapping ? __ldg(a.token_lora_mapping + f / a.topk) : 0;
+      re[it] = __ldg(a.topk_ids + f);
+    }
+  }
+}
+
+// The first of the two walks of one warp over [lo, hi), from the routing in
+// registers; the pairs' experts (-1: not this slot's, or out of range) stay
+// in ec for the second walk.  `tab` is this warp's counter row; `l` the
+// slot's LoRA index (0 without a mapping).
 __device__ __forceinline__ void warp_count_cached(const AlignArgs &a, int l, int lo, int hi, int *tab, int lane,
+                                                  const int (&rm)[kCache], const int (&re)[kCache],
                                                   int (&ec)[kCache]) {
 #pragma unroll
   for (int it = 0; it < kCache; ++it) {
     const int base = lo + it * 32;
     ec[it] = -1;
     if (base < hi) {
-      const int f = base + lane;
-      const int e = (f < hi) ? pair_expert(a, f, l, true) : -1;
+      int e = -1;
+      if (rm[it] == l) {
+        e = re[it];
+        if (e < 0 || e >= a.num_experts) {
+          flag_error(a.err, MOE_LORA_DEVERR_EXPERT_ID);
+          e = -1;
+        }
+      }
       ec[it] = e;
       const unsigned peers = __match_any_sync(0xffffffffu, e);
       if (e >= 0 && lane == __ffs(peers) - 1) tab[e] += __popc(peers);
@@ -220,19 +251,23 @@ __global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const Align
   // waits for this grid's completion before it reads any output.
   asm volatile("griddepcontrol.launch_dependents;");
 
+  const int per_warp = ((P + W - 1) / W + 31) / 32 * 32;
+  const int lo = min(P, warp * per_warp), hi = warp < W ? min(P, lo + per_warp) : lo;
+  const bool cached = per_warp <= kCache * 32;
+  // the routing goes out together with the slot's LoRA index (one round trip)
+  int rm[kCache], re[kCache];
+  if (cached) warp_load_routing(a, lo, hi, lane, rm, re);
+
   const int l = slot_lora(a, blockIdx.x, tid == 0);
   if (l < 0) return;
 
   for (int i = tid; i < W * E; i += blockDim.x) tab[i] = 0;
   __syncthreads();
 
-  const int per_warp = ((P + W - 1) / W + 31) / 32 * 32;
-  const int lo = min(P, warp * per_warp), hi = warp < W ? min(P, lo + per_warp) : lo;
-  const bool cached = per_warp <= kCache * 32;
   int *mine = tab + (warp < W ? warp : 0) * E;
   int ec[kCache];
   if (warp < W) {
-    if (cached) warp_count_cached(a, l, lo, hi, mine, lane, ec);
+    if (cached) warp_count_cached(a, a.token_lora_mapping ? l : 0, lo, hi, mine, lane, rm, re, ec);
     else warp_count(a, l, lo, hi, mine, lane);
   }
   __syncthreads();
@@ -357,6 +392,114 @@ __global__ void __launch_bounds__(kGlobalThreads) align_global_scatter_kernel(co
   warp_scatter(a, l, lo, hi, mine, a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded, lane);
 }
 
+// ----------------------------------------------------- cluster variant
+// One thread-block cluster of CA CTAs per active slot (one launch).  CTA c
+// takes the pair range [P c / CA, P (c + 1) / CA), counts it per warp (the
+// warp histograms of the shared-memory variant), and column-scans its warps.
+// The CA CTAs' per-expert counts are then read through distributed shared
+// memory: every CTA forms the slot's totals and its own starting position in
+// each segment by summing the lower ranks in rank order, so the result is
+// the same stable order as the other variants.  Expert e's sentinels and
+// block labels are written by CTA e mod CA; every CTA scatters its pairs.
+
+constexpr int kClusterAlignWarps = 32;
+constexpr int kClusterAlignThreads = kClusterAlignWarps * 32;
+constexpr int kMaxAlignCluster = 8;
+
+__global__ void __launch_bounds__(kClusterAlignThreads, 1) align_cluster_kernel(const AlignArgs a, int CA) {
+  extern __shared__ int smem[];
+  const int E = a.num_experts;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = a.M * a.topk;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int c = (int)cluster.block_rank();
+  const int z = blockIdx.x / CA;
+  int *tab = smem;                                    // [W][E] per-warp counters, then cursors
+  int *cnt = tab + kClusterAlignWarps * E;            // [E] this CTA's counts (read by peers)
+  int *before = cnt + E;                              // [E] pairs of lower-ranked CTAs
+  int *off = before + E;                              // [E + 1]
+  int *warp_sums = off + E + 1;                       // [32]
+
+  asm volatile("griddepcontrol.launch_dependents;");
+
+  const int lo_c = (int)((long long)P * c / CA), hi_c = (int)((long long)P * (c + 1) / CA);
+  const int per_warp = ((hi_c - lo_c + kClusterAlignWarps - 1) / kClusterAlignWarps + 31) / 32 * 32;
+  const int lo = min(hi_c, lo_c + warp * per_warp), hi = min(hi_c, lo + per_warp);
+  const bool cached = per_warp <= kCache * 32;
+  // the routing goes out together with the slot's LoRA index (one round trip)
+  int rm[kCache], re[kCache];
+  if (cached) warp_load_routing(a, lo, hi, lane, rm, re);
+
+  const int l = slot_lora(a, z, tid == 0 && c == 0);   // the same for every CTA of the cluster
+  if (l < 0) return;                                    // (the whole cluster returns)
+
+  for (int i = tid; i < kClusterAlignWarps * E; i += blockDim.x) tab[i] = 0;
+  __syncthreads();
+  int *mine = tab + warp * E;
+  int ec[kCache];
+  if (cached) warp_count_cached(a, a.token_lora_mapping ? l : 0, lo, hi, mine, lane, rm, re, ec);
+  else warp_count(a, l, lo, hi, mine, lane);
+  __syncthreads();
+  // column scan over this CTA's warps
+  if (tid < E) {
+    int run = 0;
+    for (int w = 0; w < kClusterAlignWarps; ++w) {
+      const int t = tab[w * E + tid];
+      tab[w * E + tid] = run;
+      run += t;
+    }
+    cnt[tid] = run;
+  }
+  // every CTA's counts are complete before any CTA reads them
+  cluster_arrive_release();
+  cluster_wait();
+  if (tid < E) {
+    int total = 0, below = 0;
+    for (int q = 0; q < CA; ++q) {
+      const int v = cluster.map_shared_rank(cnt, q)[tid];
+      total += v;
+      if (q < c) below += v;
+    }
+    before[tid] = below;
+    off[tid] = total;   // the slot's count, turned into offsets below
+  }
+  // no CTA reads a peer's counts after this: each may go on (and exit) freely
+  cluster_arrive_relaxed();
+  cluster_wait();
+  {
+    const int n_e = tid < E ? off[tid] : 0;
+    const int padded = (n_e + a.block_size - 1) / a.block_size * a.block_size;
+    int total;
+    const int excl = block_exclusive_scan(padded, warp_sums, &total);
+    __syncthreads();
+    if (tid < E) off[tid] = excl;
+    if (tid == 0) off[E] = total;
+    __syncthreads();
+    if (total > a.max_num_tokens_padded || total / a.block_size > a.max_num_m_blocks) {
+      if (tid == 0 && c == 0) {
+        flag_error(a.err, MOE_LORA_DEVERR_CAPACITY);
+        a.num_tokens_post_padded[l] = 0;
+      }
+      return;
+    }
+    if (tid == 0 && c == 0) a.num_tokens_post_padded[l] = total;
+    if (tid < E && tid % CA == c) {
+      int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
+      int32_t *experts = a.expert_ids + (size_t)l * a.max_num_m_blocks;
+      const int sentinel = a.M * a.topk;
+      for (int i = excl + n_e; i < excl + padded; ++i) sorted[i] = sentinel;
+      for (int b = excl / a.block_size; b < (excl + padded) / a.block_size; ++b) experts[b] = tid;
+    }
+  }
+  // each warp's first position in every segment
+  if (tid < E)
+    for (int w = 0; w < kClusterAlignWarps; ++w) tab[w * E + tid] += off[tid] + before[tid];
+  __syncthreads();
+  int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
+  if (cached) warp_scatter_cached(lo, hi, mine, sorted, lane, ec);
+  else warp_scatter(a, l, lo, hi, mine, sorted, lane);
+}
+
 int set_smem_limit(const void *fn, size_t bytes) {
   if (bytes <= 48 * 1024) return 0;
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) ==
@@ -394,6 +537,43 @@ int launch_align_smem(const AlignArgs &a, cudaStream_t stream) {
   if (int st = set_smem_limit((const void *)align_smem_kernel, bytes)) return st;
   align_smem_kernel<<<a.num_active_loras, threads, bytes, stream>>>(a);
   return cudaGetLastError() == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
+}
+
+int align_cluster_size(int M, int topk) {
+  // about 4096 pairs (128 per warp, kept in registers between the walks) per CTA
+  const long long P = (long long)M * topk;
+  long long ca = (P + 4095) / 4096;
+  if (ca < 1) ca = 1;
+  if (ca > kMaxAlignCluster) ca = kMaxAlignCluster;
+  int c = 1;
+  while (c < ca) c <<= 1;
+  return c;
+}
+
+bool align_cluster_fits(int E) {
+  const size_t bytes = ((size_t)kClusterAlignWarps * E + 3 * (size_t)E + 1 + 32) * sizeof(int);
+  return bytes <= 200 * 1024;
+}
+
+int launch_align_cluster(const AlignArgs &a, cudaStream_t stream) {
+  const int CA = align_cluster_size(a.M, a.topk);
+  const size_t bytes = ((size_t)kClusterAlignWarps * a.num_experts + 3 * (size_t)a.num_experts + 1 + 32) * sizeof(int);
+  if (cudaFuncSetAttribute((const void *)align_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)bytes) != cudaSuccess)
+    return MOE_LORA_ERR_LAUNCH;
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)(a.num_active_loras * CA), 1, 1);
+  lc.blockDim = dim3(kClusterAlignThreads, 1, 1);
+  lc.dynamicSmemBytes = bytes;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CA;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, align_cluster_kernel, a, CA) == cudaSuccess ? 0 : MOE_LORA_ERR_LAUNCH;
 }
 
 int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream) {

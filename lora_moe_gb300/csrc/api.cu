@@ -77,13 +77,21 @@ int check_common(int M, int topk, int E, int max_loras, int nact, int bs, int ma
 }
 
 // The shared-memory variant runs one CTA per active slot; the global variant
-// spreads each slot's pairs over many CTAs.  AUTO takes the global variant for
-// large expert counts (vLLM PR #29257, Purpose) and for long pair lists.
+// spreads each slot's pairs over many CTAs in three launches; the cluster
+// variant over up to 8 CTAs of one thread-block cluster in one launch.  AUTO
+// takes the cluster variant for large expert counts (vLLM PR #29257, Purpose:
+// the global-memory variant exists for large num_experts) and for long pair
+// lists, where it measured 10-13 us against 20-34 us for the three launches
+// and 21-47 us for one CTA per slot (prefill and large-E workloads), and the
+// shared-memory variant otherwise (3-5 us on the decode workloads, against
+// 6-7 us clustered).  The global variant is the fallback when the cluster's
+// per-warp counters do not fit in shared memory.
 int resolve_align_variant(int M, int topk, int E, int variant) {
-  if (variant == MOE_LORA_ALIGN_SMEM || variant == MOE_LORA_ALIGN_GLOBAL) return variant;
-  if (!align_smem_fits(E)) return MOE_LORA_ALIGN_GLOBAL;
-  if (E >= 256 || (long long)M * topk >= 16384) return MOE_LORA_ALIGN_GLOBAL;
-  return MOE_LORA_ALIGN_SMEM;
+  if (variant == MOE_LORA_ALIGN_SMEM || variant == MOE_LORA_ALIGN_GLOBAL || variant == MOE_LORA_ALIGN_CLUSTER)
+    return variant;
+  const bool large = !align_smem_fits(E) || E >= 256 || (long long)M * topk >= 16384;
+  if (!large) return MOE_LORA_ALIGN_SMEM;
+  return align_cluster_fits(E) ? MOE_LORA_ALIGN_CLUSTER : MOE_LORA_ALIGN_GLOBAL;
 }
 
 }  // namespace
@@ -98,12 +106,13 @@ static int align_impl(const int32_t *topk_ids, const int32_t *token_lora_mapping
   if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
                             max_num_m_blocks))
     return st;
-  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_GLOBAL) return MOE_LORA_ERR_INVALID_ARG;
+  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_CLUSTER) return MOE_LORA_ERR_INVALID_ARG;
   if (num_active_loras == 0) return MOE_LORA_OK;
   if (!sorted_token_ids || !expert_ids || !num_tokens_post_padded) return MOE_LORA_ERR_INVALID_ARG;
   if (M > 0 && !topk_ids) return MOE_LORA_ERR_INVALID_ARG;
   const int v = resolve_align_variant(M, topk, num_experts, variant);
   if (v == MOE_LORA_ALIGN_SMEM && !align_smem_fits(num_experts)) return MOE_LORA_ERR_UNSUPPORTED;
+  if (v == MOE_LORA_ALIGN_CLUSTER && !align_cluster_fits(num_experts)) return MOE_LORA_ERR_UNSUPPORTED;
   DeviceInfo dev;
   if (int st = current_device_info(&dev)) return st;
   AlignArgs a;
@@ -125,6 +134,7 @@ static int align_impl(const int32_t *topk_ids, const int32_t *token_lora_mapping
   a.max_num_m_blocks = max_num_m_blocks;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (v == MOE_LORA_ALIGN_SMEM) return launch_align_smem(a, s);
+  if (v == MOE_LORA_ALIGN_CLUSTER) return launch_align_cluster(a, s);
   const size_t need = align_global_workspace_bytes(M, topk, num_experts, num_active_loras);
   if (!workspace || workspace_bytes < need) return MOE_LORA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return MOE_LORA_ERR_MISALIGNED;
@@ -264,7 +274,7 @@ int check_align_args(const int32_t *topk_ids, const int32_t *token_lora_mapping,
   if (int st = check_common(M, topk, num_experts, max_loras, num_active_loras, block_size, max_num_tokens_padded,
                             max_num_m_blocks))
     return st;
-  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_GLOBAL) return MOE_LORA_ERR_INVALID_ARG;
+  if (variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_CLUSTER) return MOE_LORA_ERR_INVALID_ARG;
   if (M > 0 && num_active_loras > 0 && !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
   if (num_active_loras > 0 && !lora_ids) return MOE_LORA_ERR_INVALID_ARG;
   if (num_active_loras == 0) return MOE_LORA_OK;
@@ -302,6 +312,17 @@ int moe_lora_max_num_m_blocks(int M, int topk, int num_experts, int block_size) 
   const int cap = moe_lora_max_num_tokens_padded(M, topk, num_experts, block_size);
   if (cap < 0) return -1;
   return (cap + block_size - 1) / block_size;
+}
+
+int moe_lora_align_resolve_variant(int M, int topk, int num_experts, int variant) {
+  if (M < 0 || topk < 1 || num_experts < 1 || variant < MOE_LORA_ALIGN_AUTO || variant > MOE_LORA_ALIGN_CLUSTER)
+    return -MOE_LORA_ERR_INVALID_ARG;
+  if (num_experts > kMaxExperts || topk > num_experts) return -MOE_LORA_ERR_UNSUPPORTED;
+  const int v = resolve_align_variant(M, topk, num_experts, variant);
+  if ((v == MOE_LORA_ALIGN_SMEM && !align_smem_fits(num_experts)) ||
+      (v == MOE_LORA_ALIGN_CLUSTER && !align_cluster_fits(num_experts)))
+    return -MOE_LORA_ERR_UNSUPPORTED;
+  return v;
 }
 
 size_t moe_lora_align_workspace_bytes(int M, int topk, int num_experts, int num_active_loras, int block_size,

@@ -91,6 +91,11 @@ int check_align_args(const int32_t *topk_ids, const int32_t *token_lora_mapping,
                      int variant);
 
 int launch_align_smem(const AlignArgs &a, cudaStream_t stream);
+// The cluster variant: CTAs per slot for these sizes, whether its shared
+// memory holds the per-warp counters of E experts, and the launch.
+int align_cluster_size(int M, int topk);
+bool align_cluster_fits(int E);
+int launch_align_cluster(const AlignArgs &a, cudaStream_t stream);
 int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream);
 int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream);
 // Naive block assignment: one work item per pair, no align outputs.

@@ -133,7 +133,7 @@ def test_default_workload_and_config_list():
     assert a.workload == "large_e_nact8" and a.configs == "all" and a.min_regions >= 5
 
 
-@pytest.mark.parametrize("v,name", [(0, None), (1, "smem (forced)"), (2, "global (forced)")])
+@pytest.mark.parametrize("v,name", [(0, None), (1, "smem (forced)"), (2, "global (forced)"), (3, "cluster (forced)")])
 def test_forced_align_variant_is_named_in_the_config(monkeypatch, v, name):
     import sys
     monkeypatch.setattr(sys, "argv", ["bench.py", "--align-variant", str(v)])

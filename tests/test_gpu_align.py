@@ -8,7 +8,7 @@ from lora_moe_gb300 import inputs as gen
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [B.ALIGN_SMEM, B.ALIGN_GLOBAL]
+VARIANTS = [B.ALIGN_SMEM, B.ALIGN_GLOBAL, B.ALIGN_CLUSTER]
 WORKLOADS = ["tiny", "decode_qwen3_w13", "decode_gptoss_w2", "prefill_mixtral_w13",
              "large_e_nact1", "large_e_nact4", "large_e_nact8"]
 
@@ -82,6 +82,18 @@ def test_align_bad_ids_flagged_and_dropped(variant):
         (np.array([[0]], np.int32), np.array([0], np.int32), np.array([5], np.int32)), 4, 2, 16, variant)
     assert err & B.DEVERR_LORA_ID
     assert (n == 0x7FFFFFFF).all()
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("M,topk,E", [(20000, 8, 64), (4097, 1, 1024), (9000, 7, 256)])
+def test_align_long_pair_lists(M, topk, E, variant):
+    """Pair lists long enough for 8-CTA clusters and, past 256 pairs a warp,
+    the walks that reread the routing; ragged ranges per CTA and per warp."""
+    from helpers import assert_align_equal
+    rng = np.random.default_rng(M + E)
+    topk_ids = np.stack([rng.choice(E, topk, replace=False) for _ in range(M)]).astype(np.int32)
+    mapping = rng.integers(-1, 3, size=M).astype(np.int32)
+    assert_align_equal(topk_ids, mapping, np.array([2, 0], np.int32), E, 3, 64, variant)
 
 
 @pytest.mark.parametrize("variant", VARIANTS)

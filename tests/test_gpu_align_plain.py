@@ -10,7 +10,7 @@ from lora_moe_gb300 import inputs as gen
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [B.ALIGN_SMEM, B.ALIGN_GLOBAL, B.ALIGN_AUTO]
+VARIANTS = [B.ALIGN_SMEM, B.ALIGN_GLOBAL, B.ALIGN_CLUSTER, B.ALIGN_AUTO]
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -166,7 +166,7 @@ def test_fused_no_covered_pairs(path):
     assert err == 0 and np.array_equal(host_bf16_bits(y).reshape(inp.y_in.shape), inp.y_in)
 
 
-@pytest.mark.parametrize("variant", [B.ALIGN_SMEM, B.ALIGN_GLOBAL])
+@pytest.mark.parametrize("variant", [B.ALIGN_SMEM, B.ALIGN_GLOBAL, B.ALIGN_CLUSTER])
 def test_fused_after_either_align_variant(variant):
     inp = gen.make_inputs(gen.WORKLOADS["decode_gptoss_w2"])
     run_and_compare_full(inp, B.PATH_AUTO, variant=variant)

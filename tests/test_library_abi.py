@@ -61,7 +61,8 @@ def test_workspace_sizes():
     n = B.align_workspace_bytes(4096, 8, 256, 8, 64, B.ALIGN_GLOBAL)
     assert n > 0 and n % (8 * 4) == 0
     assert B.align_workspace_bytes(4096, 8, 256, 4, 64, B.ALIGN_GLOBAL) * 2 == n
-    assert B.align_workspace_bytes(4096, 8, 256, 8, 64, B.ALIGN_AUTO) == n   # AUTO picks global at E=256
+    assert B.align_workspace_bytes(4096, 8, 256, 8, 64, B.ALIGN_AUTO) == 0   # AUTO picks the cluster variant at E=256
+    assert B.align_workspace_bytes(4096, 8, 256, 8, 64, B.ALIGN_CLUSTER) == 0
 
 
 def test_version():
@@ -193,6 +194,16 @@ def test_fused_resolve_path():
     assert R(16, 8, 128, 2048, 1536, 24, 2, 16, 1, 4) == -2  # streaming: ranks 8, 16, 32, 64, 128
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 5, 0) == -1  # too many slices
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 9) == -1
+
+
+def test_align_resolve_variant():
+    R = B.lib().moe_lora_align_resolve_variant
+    assert R(16, 8, 128, 0) in (1, 2, 3)          # AUTO resolves to a concrete variant
+    for v in (1, 2, 3):
+        assert R(16, 8, 128, v) == v               # forced variants are kept
+    assert R(16, 8, 1025, 0) == -2                 # num_experts > 1024
+    assert R(16, 8, 128, 4) == -1                  # no such variant
+    assert R(-1, 8, 128, 0) == -1
 
 
 def test_plain_align_argument_errors():
