@@ -140,12 +140,13 @@ def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weigh
 NCU_TRAFFIC = {
     ("decode_qwen3_w13", "fused_cuda_core_kernel"): 5573632,      # fused_cuda_core_decode_qwen3_w13.md
     ("decode_gptoss_w2", "fused_tcgen05_kernel"): 170909184,      # fused_tcgen05_decode_gptoss_w2.md
+    ("decode_gptoss_w2", "fused_cluster_stream_kernel"): 155535104,  # fused_cluster_stream_decode_gptoss_w2.md
     ("large_e_l1", "fused_tcgen05_kernel"): 1080333056,           # fused_tcgen05_large_e_l1.md
     # the same active work as large_e_l1 (the inactive slots are never read)
     ("large_e_nact1", "fused_tcgen05_kernel"): 1080333056,        # fused_tcgen05_large_e_l1.md
+    ("large_e_nact8", "fused_tcgen05_kernel"): 6153373440,        # fused_tcgen05_large_e_nact8_traffic.md
     ("prefill_mixtral_w13_m2048", "fused_tcgen05_kernel"): 468284416,  # fused_tcgen05_prefill_mixtral_w13_m2048.md
-    # scaled from the M = 2048 capture: 0.90 of the algorithmic bytes
-    ("prefill_mixtral_w13", "fused_tcgen05_kernel"): 1782400000,  # fused_tcgen05_prefill_mixtral_w13_m2048.md
+    ("prefill_mixtral_w13", "fused_tcgen05_kernel"): 2211975168,  # fused_tcgen05_prefill_mixtral_w13_traffic.md
 }
 
 
@@ -565,11 +566,12 @@ def config_entry(rig, counts, peak, tc_peak, seconds):
     rig.check_err()
     gbs = counts["fused_bytes"] / (fused_us * 1e-6) / 1e9
     tflops = counts["flops"] / (fused_us * 1e-6) / 1e12
-    return dict({"kernel": kernel_name_of(B, w, rig.args), "step_us": step_us, "fused_us": fused_us,
+    kname = kernel_name_of(B, w, rig.args)
+    return dict({"kernel": kname, "step_us": step_us, "fused_us": fused_us,
                  "fused_gbs": gbs, "fused_tflops": tflops, "frac_hbm": gbs / peak,
                  "frac_bf16_tensor": tflops / tc_peak,
                  "fused_bytes": counts["fused_bytes"], "flops": counts["flops"], "pairs": counts["pairs"],
-                 "blocks": counts["blocks"]}, **align)
+                 "blocks": counts["blocks"], "traffic_ncu": NCU_TRAFFIC.get((w.name, kname))}, **align)
 
 
 def run_ours(args, world, rank, local, pg):
