@@ -44,6 +44,10 @@
  *     NULL), readable after the stream has synchronised; the offending entry is
  *     skipped, never dereferenced.
  *   - Every (token, top-k) pair is named by its flat index f = m*topk + k.
+ *   - A fused call may start while the align call before it on the same
+ *     stream is finishing (programmatic dependent launch); it reads the
+ *     align's outputs only after that kernel has completed, and lora_ids /
+ *     adapter_enabled, which the align does not write, possibly earlier.
  */
 #ifndef MOE_LORA_H
 #define MOE_LORA_H
@@ -321,6 +325,35 @@ int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair,
                                        int num_experts, int K, int N, int rank, int max_loras,
                                        int num_active_loras, int add_inputs, int path,
                                        int32_t *err_flag, void *stream);
+
+/*
+ * moe_lora_test_withheld_copy -- a test of the library's bounded waits, not
+ * for production use.  The pages have no counterpart: it exists so that a
+ * test can make one of the kernels' on-chip waits run out without faulting or
+ * hanging the GPU.  It is moe_lora_fused_shrink_expand_naive on the
+ * one-cluster-per-pair kernel (MOE_LORA_PATH_CUDA_CORE_CLUSTER), except that
+ * no CTA issues the bulk copy of its slice of B[l][e], whose arrival it then
+ * waits for with a limit of wait_limit_ns nanoseconds (1000 .. 4e9) instead
+ * of 4 s.  Every CTA that reaches a covered pair's wait gives up after the
+ * limit, ORs MOE_LORA_DEVERR_TIMEOUT into *err_flag, requests no further
+ * copy, runs its remaining control flow (its cluster barriers stay balanced)
+ * and exits; the call completes.  No copy is in flight when a CTA exits (the
+ * withheld one was never issued), so the device stays usable.  The covered
+ * pairs' output columns are left in an unspecified state; everything else in
+ * y is untouched.  Arguments and argument errors as for the naive entry point,
+ * plus MOE_LORA_ERR_INVALID_ARG for a limit outside the range.
+ */
+int moe_lora_test_withheld_copy(const moe_lora_bf16 *x, int x_per_pair,
+                                const moe_lora_bf16 *const *lora_a,
+                                const moe_lora_bf16 *const *lora_b, int num_slices,
+                                moe_lora_bf16 *y, int ldy, int y_offset,
+                                const float *topk_weights, const int32_t *topk_ids,
+                                const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                                const int32_t *adapter_enabled, int M, int topk,
+                                int num_experts, int K, int N, int rank, int max_loras,
+                                int num_active_loras, int add_inputs,
+                                unsigned long long wait_limit_ns, int32_t *err_flag,
+                                void *stream);
 
 /*
  * moe_lora_fused_resolve_path -- the kernel a fused call with these sizes

@@ -74,6 +74,9 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_fused_shrink_expand_naive.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P), I, P, I, I,
                                                              P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, P,
                                                              P]
+            L.moe_lora_test_withheld_copy.restype = I
+            L.moe_lora_test_withheld_copy.argtypes = [P, I, ctypes.POINTER(P), ctypes.POINTER(P), I, P, I, I, P, P,
+                                                      P, P, P, I, I, I, I, I, I, I, I, I, ctypes.c_ulonglong, P, P]
             L.moe_lora_fused_plan.restype = I
             L.moe_lora_fused_plan.argtypes = [I] * 12 + [P]
             L.moe_lora_fused_resolve_path.restype = I
@@ -312,6 +315,28 @@ def moe_lora_fused_shrink_expand_naive(x, lora_a, lora_b, y, topk_ids, token_lor
         _ptr(adapter_enabled, torch.int32, "adapter_enabled"), M, topk, E, K, N, r, L, lora_ids.numel(),
         int(bool(add_inputs)), int(path), _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
     _check(st, "moe_lora_fused_shrink_expand_naive")
+
+
+def moe_lora_test_withheld_copy(x, lora_a, lora_b, y, topk_ids, token_lora_mapping, lora_ids, max_loras,
+                                wait_limit_ns, add_inputs=True, err_flag=None, stream=None):
+    """moe_lora_test_withheld_copy (a test of the bounded waits): the naive call
+    with every CTA's B-slice copy withheld and its wait limited to
+    wait_limit_ns; y [M, topk, N], one slice."""
+    if isinstance(lora_a, torch.Tensor):
+        lora_a, lora_b = [lora_a], [lora_b]
+    S = len(lora_a)
+    L, E, r, K = lora_a[0].shape
+    N = lora_b[0].shape[2]
+    M, topk = topk_ids.shape
+    bf = torch.bfloat16
+    a_ptrs = (ctypes.c_void_p * S)(*[_ptr(a, bf, "lora_a") for a in lora_a])
+    b_ptrs = (ctypes.c_void_p * S)(*[_ptr(b, bf, "lora_b") for b in lora_b])
+    st = lib().moe_lora_test_withheld_copy(
+        _ptr(x, bf, "x"), 0, a_ptrs, b_ptrs, S, _ptr(y, bf, "y"), y.shape[2], 0, None,
+        _ptr(topk_ids, torch.int32, "topk_ids"), _ptr(token_lora_mapping, torch.int32, "token_lora_mapping"),
+        _ptr(lora_ids, torch.int32, "lora_ids"), None, M, topk, E, K, N, r, L, lora_ids.numel(),
+        int(bool(add_inputs)), int(wait_limit_ns), _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
+    _check(st, "moe_lora_test_withheld_copy")
 
 
 class AlignBuffers:

@@ -285,6 +285,38 @@ int check_align_args(const int32_t *topk_ids, const int32_t *token_lora_mapping,
 
 }  // namespace moe_lora
 
+static int naive_impl(const moe_lora_bf16 *x, int x_per_pair, const moe_lora_bf16 *const *lora_a,
+                                       const moe_lora_bf16 *const *lora_b, int num_slices, moe_lora_bf16 *y,
+                                       int ldy, int y_offset, const float *topk_weights, const int32_t *topk_ids,
+                                       const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                                       const int32_t *adapter_enabled, int M, int topk, int num_experts, int K,
+                                       int N, int rank, int max_loras, int num_active_loras, int add_inputs,
+                                       int path, int32_t *err_flag, void *stream,
+                                       unsigned long long wait_limit_ns = 0, int withhold_b = 0) {
+  if (M < 0 || topk < 1 || num_experts < 1 || max_loras < 1 || num_active_loras < 0) return MOE_LORA_ERR_INVALID_ARG;
+  if (path != MOE_LORA_PATH_AUTO && path != MOE_LORA_PATH_CUDA_CORE && path != MOE_LORA_PATH_CUDA_CORE_CLUSTER &&
+      path != MOE_LORA_PATH_CUDA_CORE_STREAM)
+    return MOE_LORA_ERR_INVALID_ARG;
+  if (!path_takes_rank(path, rank)) return MOE_LORA_ERR_UNSUPPORTED;
+  if (num_experts > kMaxExperts || topk > num_experts) return MOE_LORA_ERR_UNSUPPORTED;
+  if (num_active_loras > max_loras) return MOE_LORA_ERR_INVALID_ARG;
+  if ((long long)M * topk > INT32_MAX / 2) return MOE_LORA_ERR_UNSUPPORTED;
+  FusedArgs f;
+  bool empty = false;
+  if (int st = prepare_fused(x, x_per_pair, lora_a, lora_b, num_slices, y, ldy, y_offset, topk_weights, lora_ids,
+                             adapter_enabled, M, topk, num_experts, K, N, rank, max_loras, num_active_loras,
+                             add_inputs, err_flag, &f, &empty))
+    return st;
+  if (empty) return MOE_LORA_OK;
+  if (!topk_ids || !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
+  f.topk_ids = topk_ids;
+  f.token_lora_mapping = token_lora_mapping;
+  const int use = resolve_naive_path(f, path);
+  if (use < 0) return -use;
+  if (use == MOE_LORA_PATH_CUDA_CORE_STREAM) return launch_fused_cluster_stream_naive(f, static_cast<cudaStream_t>(stream));
+  return launch_fused_naive(f, static_cast<cudaStream_t>(stream), wait_limit_ns, withhold_b);
+}
+
 extern "C" {
 
 int moe_lora_version(void) { return 100; }
@@ -462,28 +494,23 @@ int moe_lora_fused_shrink_expand_naive(const moe_lora_bf16 *x, int x_per_pair, c
                                        const int32_t *adapter_enabled, int M, int topk, int num_experts, int K,
                                        int N, int rank, int max_loras, int num_active_loras, int add_inputs,
                                        int path, int32_t *err_flag, void *stream) {
-  if (M < 0 || topk < 1 || num_experts < 1 || max_loras < 1 || num_active_loras < 0) return MOE_LORA_ERR_INVALID_ARG;
-  if (path != MOE_LORA_PATH_AUTO && path != MOE_LORA_PATH_CUDA_CORE && path != MOE_LORA_PATH_CUDA_CORE_CLUSTER &&
-      path != MOE_LORA_PATH_CUDA_CORE_STREAM)
-    return MOE_LORA_ERR_INVALID_ARG;
-  if (!path_takes_rank(path, rank)) return MOE_LORA_ERR_UNSUPPORTED;
-  if (num_experts > kMaxExperts || topk > num_experts) return MOE_LORA_ERR_UNSUPPORTED;
-  if (num_active_loras > max_loras) return MOE_LORA_ERR_INVALID_ARG;
-  if ((long long)M * topk > INT32_MAX / 2) return MOE_LORA_ERR_UNSUPPORTED;
-  FusedArgs f;
-  bool empty = false;
-  if (int st = prepare_fused(x, x_per_pair, lora_a, lora_b, num_slices, y, ldy, y_offset, topk_weights, lora_ids,
-                             adapter_enabled, M, topk, num_experts, K, N, rank, max_loras, num_active_loras,
-                             add_inputs, err_flag, &f, &empty))
-    return st;
-  if (empty) return MOE_LORA_OK;
-  if (!topk_ids || !token_lora_mapping) return MOE_LORA_ERR_INVALID_ARG;
-  f.topk_ids = topk_ids;
-  f.token_lora_mapping = token_lora_mapping;
-  const int use = resolve_naive_path(f, path);
-  if (use < 0) return -use;
-  if (use == MOE_LORA_PATH_CUDA_CORE_STREAM) return launch_fused_cluster_stream_naive(f, static_cast<cudaStream_t>(stream));
-  return launch_fused_naive(f, static_cast<cudaStream_t>(stream));
+  return naive_impl(x, x_per_pair, lora_a, lora_b, num_slices, y, ldy, y_offset, topk_weights, topk_ids,
+                    token_lora_mapping, lora_ids, adapter_enabled, M, topk, num_experts, K, N, rank, max_loras,
+                    num_active_loras, add_inputs, path, err_flag, stream);
+}
+
+int moe_lora_test_withheld_copy(const moe_lora_bf16 *x, int x_per_pair, const moe_lora_bf16 *const *lora_a,
+                                const moe_lora_bf16 *const *lora_b, int num_slices, moe_lora_bf16 *y, int ldy,
+                                int y_offset, const float *topk_weights, const int32_t *topk_ids,
+                                const int32_t *token_lora_mapping, const int32_t *lora_ids,
+                                const int32_t *adapter_enabled, int M, int topk, int num_experts, int K, int N,
+                                int rank, int max_loras, int num_active_loras, int add_inputs,
+                                unsigned long long wait_limit_ns, int32_t *err_flag, void *stream) {
+  if (wait_limit_ns < 1000ull || wait_limit_ns > 4000000000ull) return MOE_LORA_ERR_INVALID_ARG;
+  return naive_impl(x, x_per_pair, lora_a, lora_b, num_slices, y, ldy, y_offset, topk_weights, topk_ids,
+                    token_lora_mapping, lora_ids, adapter_enabled, M, topk, num_experts, K, N, rank, max_loras,
+                    num_active_loras, add_inputs, MOE_LORA_PATH_CUDA_CORE_CLUSTER, err_flag, stream, wait_limit_ns,
+                    1);
 }
 
 int moe_lora_fused_shrink_expand(const moe_lora_bf16 *x, const moe_lora_bf16 *lora_a, const moe_lora_bf16 *lora_b,

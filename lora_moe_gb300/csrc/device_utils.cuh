@@ -138,6 +138,23 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t r
                : "memory");
 }
 
+// mbar_wait with a caller-chosen limit in nanoseconds (instead of
+// kWaitTimeoutNs).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, volatile int *abort, int32_t *err,
+                                              unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+    if (*abort) return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      flag_error(err, MOE_LORA_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // ------------------------------------------------------------ async copies
 
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.

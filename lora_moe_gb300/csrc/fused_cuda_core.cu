@@ -61,6 +61,8 @@ struct CcCfg {
   int off_a, off_x, off_b, off_y, off_tp, off_t;
   int smem_bytes;
   int lpr_log2;        // expand: lanes per B row, log2
+  unsigned long long wait_limit_ns;   // limit of the wait for the B slice (kWaitTimeoutNs)
+  int withhold_b;      // test of the bounded wait: the B slice's copy is never issued
   // cluster rank c's slices: K columns [k_lo, k_lo + kn), N rows [n_lo, n_lo + nn)
   int k_lo[kMaxCluster], kn[kMaxCluster], n_lo[kMaxCluster], nn[kMaxCluster];
 };
@@ -103,16 +105,20 @@ __device__ __forceinline__ float dot8(const float (&a)[8], const uint4 xv) {
 // Request this CTA's slices of A[l][e] (rows j, columns [k_lo, k_lo + 8 kch),
 // by cp.async) and of B[l][e] (rows [n_lo, n_lo + nn), one bulk copy) as soon
 // as the expert is known; x and y_in rows follow once the pairs are.
+// After a wait has given up (*abort) nothing more is requested: the CTA's
+// barrier may still be in a phase that never completed, and no copy may be
+// left in flight when it exits.
 __device__ __forceinline__ void request_adapters(const FusedArgs &p, const CcCfg &cfg, Meta &meta, uint8_t *a_s,
                                                  uint8_t *b_s, int l, int e, int sl, int k_lo, int kch, int n_lo,
                                                  int nn) {
+  if (__syncthreads_or(meta.abort)) return;
   const int r = p.rank, K = p.K, N = p.N;
   const size_t le = (size_t)l * p.num_experts + e;
   const uint16_t *A = slice_a(p, sl) + le * r * K;
   const uint16_t *Bm = slice_b(p, sl) + le * N * r;
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&meta.bar, (uint32_t)nn * r * 2);
-    bulk_g2s(b_s, Bm + (size_t)n_lo * r, (uint32_t)nn * r * 2, &meta.bar);
+    if (!cfg.withhold_b) bulk_g2s(b_s, Bm + (size_t)n_lo * r, (uint32_t)nn * r * 2, &meta.bar);
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int j = warp; j < r; j += kWarps)
@@ -256,7 +262,7 @@ __device__ __forceinline__ void run_group(const GroupCtx &g, int g0, int nvg) {
     }
   }
   __syncthreads();
-  if (g0 == 0) mbar_wait(&meta.bar, phase, abort, p.err);
+  if (g0 == 0) mbar_wait_for(&meta.bar, phase, abort, p.err, cfg.wait_limit_ns);
 
   // ---- expand: y rows of this CTA's N-slice.  A B row is read by lpr
   // lanes (one shared-memory vector each); their partial sums meet by
@@ -353,16 +359,23 @@ __global__ void __launch_bounds__(kThreads, 4) fused_cuda_core_kernel(const Fuse
   const int k_lo = cfg.k_lo[c], kn = cfg.kn[c], n_lo = cfg.n_lo[c], nn = cfg.nn[c];
   const int kch = kn / 8, nch = nn / 8;
 
-  wait_for_prior_grid();   // every input is read from here on
-  int l = 0, nitems = P, e_first = 0, f_first = -1;
+  // The slot's LoRA index and enable flag are inputs the align does not
+  // write: they are read before waiting for it.  Everything else is read
+  // after griddepcontrol.wait.
+  int l = 0, en = 1;
+  if (!NAIVE) {
+    l = __ldg(p.lora_ids + z);
+    if (l >= 0 && l < p.max_loras && p.adapter_enabled) en = __ldg(p.adapter_enabled + l);
+  }
+  wait_for_prior_grid();   // the align outputs are read from here on
+  int nitems = P, e_first = 0, f_first = -1;
   if (!NAIVE) {
     // Uniform over the cluster: every CTA of it reads the same values.
-    l = __ldg(p.lora_ids + z);
     if (l < 0 || l >= p.max_loras) {
       if (c == 0 && tid == 0 && blockIdx.z == 0 && sl == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
       return;
     }
-    if (p.adapter_enabled && __ldg(p.adapter_enabled + l) == 0) return;
+    if (en == 0) return;
     // The first block's expert and pair ids are requested together with the
     // slot's block count (one round trip); they are only used if the block exists.
     const int b_first = blockIdx.z;
@@ -446,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 4) fused_cuda_core_kernel(const Fuse
       // nothing to apply; the requested slices must land before their buffers
       // are reused or the CTA exits
       cp_async_wait_group<0>();
-      mbar_wait(&meta.bar, phase, abort, p.err);
+      mbar_wait_for(&meta.bar, phase, abort, p.err, cfg.wait_limit_ns);
       phase ^= 1;
       __syncthreads();
       continue;
@@ -486,6 +499,8 @@ bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, int pg, CcCfg *cfg
   int lg = 0;
   while ((1 << lg) < vecs && lg < 4) ++lg;
   cfg->lpr_log2 = lg;
+  cfg->wait_limit_ns = kWaitTimeoutNs;
+  cfg->withhold_b = 0;
   size_t off = (sizeof(Meta) + 127) / 128 * 128;
   cfg->off_a = (int)off;
   off += (size_t)r * cfg->a_pitch;
@@ -653,11 +668,13 @@ int plan_fused_cuda_core(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *o
   return 0;
 }
 
-int launch_fused_naive(const FusedArgs &f, cudaStream_t stream) {
+int launch_fused_naive(const FusedArgs &f, cudaStream_t stream, unsigned long long wait_limit_ns, int withhold_b) {
   DeviceInfo dev;
   if (int st = current_device_info(&dev)) return st;
   CcCfg cfg;
   if (int st = pick_cfg(f, dev, 1, &cfg)) return st;
+  if (wait_limit_ns) cfg.wait_limit_ns = wait_limit_ns;
+  cfg.withhold_b = withhold_b;
   // grid (C, slices, pairs), as the one-program-per-pair grid of the naive
   // assignment; past a few waves, CTAs walk several pairs.
   // Every pair gets its own cluster (uncovered ones exit at once and free

@@ -98,8 +98,11 @@ bool align_cluster_fits(int E);
 int launch_align_cluster(const AlignArgs &a, cudaStream_t stream);
 int launch_align_global(const AlignArgs &a, void *workspace, cudaStream_t stream);
 int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream);
-// Naive block assignment: one work item per pair, no align outputs.
-int launch_fused_naive(const FusedArgs &f, cudaStream_t stream);
+// Naive block assignment: one work item per pair, no align outputs.  For the
+// test of the bounded waits only: wait_limit_ns (0: the default 4 s) bounds the
+// wait for each CTA's B slice, and withhold_b leaves that copy unissued.
+int launch_fused_naive(const FusedArgs &f, cudaStream_t stream, unsigned long long wait_limit_ns = 0,
+                       int withhold_b = 0);
 int launch_fused_tcgen05(const FusedArgs &f, cudaStream_t stream);
 // Whether the tensor-core path takes these arguments (rank % 8 == 0, at most
 // 128 listed slots).
