@@ -15,6 +15,10 @@ namespace moe_lora {
 
 // A bounded wait gives up after this long and reports MOE_LORA_DEVERR_TIMEOUT.
 constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;
+// Longest a waiting thread sleeps in one try_wait before it looks at the abort
+// flag and the clock again.  The thread wakes as soon as the phase completes;
+// the hint only spares the issue slots that polling would take.
+constexpr uint32_t kSuspendHintNs = 20000u;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -63,6 +67,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return done != 0;
 }
 
+// try_wait that may suspend the thread for up to kSuspendHintNs.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return done != 0;
+}
+
 // Wait for the phase with the given parity to complete.  Gives up after
 // kWaitTimeoutNs, or at once if *abort is set; on giving up it sets *abort and
 // the TIMEOUT bit.  Returns false when it gave up.  A CTA that gave up keeps
@@ -74,7 +91,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volati
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     if (*abort) return false;
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitTimeoutNs) {
       *abort = 1;
       flag_error(err, MOE_LORA_DEVERR_TIMEOUT);
@@ -97,13 +114,24 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
       : "memory");
   return done != 0;
 }
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return done != 0;
+}
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort,
                                                   int32_t *err) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     if (*abort) return false;
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_try_wait_cluster_sleep(bar, parity)) return true;
     if (global_timer_ns() - t0 > kWaitTimeoutNs) {
       *abort = 1;
       flag_error(err, MOE_LORA_DEVERR_TIMEOUT);
@@ -128,6 +156,14 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
 
+// Arrive on the mbarrier at shared::cluster address `rbar` without release
+// semantics: it does not wait for this thread's outstanding global stores.
+// For hand-backs of a shared buffer whose reads are already complete (their
+// values consumed before a CTA barrier that precedes the arrive).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
+
 // Asynchronous 16-byte store into a peer's (or this CTA's) shared memory at
 // shared::cluster address `raddr`; its bytes are counted as completed
 // transactions on the mbarrier at shared::cluster address `rbar` of the same CTA.
@@ -146,7 +182,7 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, vo
   const unsigned long long t0 = global_timer_ns();
   while (true) {
     if (*abort) return false;
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
       flag_error(err, MOE_LORA_DEVERR_TIMEOUT);

@@ -55,7 +55,7 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarps = 2;           // stage it is issued by producer warp it % 2
 constexpr int kThreads = kConsumers + kProducerWarps * 32;
-constexpr int kNPG = 4;                     // pairs per work item
+constexpr int kNPG = 2;                     // pairs per work item
 constexpr int kDesc = 8;                    // work-item descriptors in flight
 constexpr int kMaxStages = 24;
 constexpr int kMaxCluster = 8;
@@ -112,31 +112,35 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kWaitTimeoutNs) return;
 }
 
-// sum_i a[i] * b[i] over one 16-byte vector of bf16 pairs (fp32)
-__device__ __forceinline__ float dot8_bf16(const uint4 a, const uint4 b) {
-  const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    s = fmaf(__uint_as_float(wa[i] << 16), __uint_as_float(wb[i] << 16), s);
-    s = fmaf(__uint_as_float(wa[i] & 0xFFFF0000u), __uint_as_float(wb[i] & 0xFFFF0000u), s);
-  }
-  return s;
-}
+// Packed pairs of fp32 (f32x2) in a 64-bit register: the arithmetic runs two
+// lanes of a vector per instruction (fma.rn.f32x2).
+typedef unsigned long long f32x2;
 
-// sum_i b[i] * t[i] over one 16-byte vector of bf16 and eight fp32 (shared)
-__device__ __forceinline__ float dot8_bf16_f32(const uint4 b, const float *t) {
-  const float4 t0 = *reinterpret_cast<const float4 *>(t);
-  const float4 t1 = *reinterpret_cast<const float4 *>(t + 4);
-  float s = __uint_as_float(b.x << 16) * t0.x;
-  s = fmaf(__uint_as_float(b.x & 0xFFFF0000u), t0.y, s);
-  s = fmaf(__uint_as_float(b.y << 16), t0.z, s);
-  s = fmaf(__uint_as_float(b.y & 0xFFFF0000u), t0.w, s);
-  s = fmaf(__uint_as_float(b.z << 16), t1.x, s);
-  s = fmaf(__uint_as_float(b.z & 0xFFFF0000u), t1.y, s);
-  s = fmaf(__uint_as_float(b.w << 16), t1.z, s);
-  s = fmaf(__uint_as_float(b.w & 0xFFFF0000u), t1.w, s);
-  return s;
+__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2_sum(f32x2 v) {
+  float lo, hi;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  return lo + hi;
+}
+// the two bf16 of a 32-bit word, widened (exactly) to fp32
+__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+__device__ __forceinline__ f32x2 ffma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// one 16-byte vector of bf16 as four f32x2
+__device__ __forceinline__ void unpack_v(const uint4 v, f32x2 (&f)[4]) {
+  f[0] = bf2_to_f2(v.x);
+  f[1] = bf2_to_f2(v.y);
+  f[2] = bf2_to_f2(v.z);
+  f[3] = bf2_to_f2(v.w);
 }
 
 __device__ __forceinline__ int find_slot(const int *prefix, int nact, int item) {
@@ -408,6 +412,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     float *tfull = reinterpret_cast<float *>(smem + cfg.off_tfull);
     float *stg = reinterpret_cast<float *>(smem + cfg.off_stg);
     uint32_t it = 0;
+    uint32_t cst = 0, cph = 0;   // it % NS and (it / NS) & 1, kept without a division
+    auto advance = [&] {
+      ++it;
+      if (++cst == (uint32_t)NS) {
+        cst = 0;
+        cph ^= 1;
+      }
+    };
     // the previous item, whose exchange overlaps this item's shrink
     bool have_prev = false;
     uint32_t pv_item = 0;
@@ -435,33 +447,69 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tf[i] = sum;
       }
       named_barrier(1, kConsumers);
-      // this CTA's buffer b is free again: tell every CTA of the cluster
+      // this CTA's buffer b is free again: tell every CTA of the cluster.  The
+      // reads of rbuf above are complete (their sums were stored before the
+      // barrier), so the arrive needs no release, which would first wait for
+      // this thread's y stores still in flight.
       if (tid == 0)
-        for (int dst = 0; dst < C; ++dst) mbar_arrive_remote(cluster_map(smem_addr(&meta.t_free[b]), dst));
+        for (int dst = 0; dst < C; ++dst) mbar_arrive_remote_relaxed(cluster_map(smem_addr(&meta.t_free[b]), dst));
       // ---- expand: this CTA's output rows
       const int col0 = p.y_offset + s * N;
-      for (int n0 = n_lo; n0 < n_hi; n0 += nb, ++it) {
-        const int st = it % NS;
-        mbar_wait(&meta.full[st], (it / NS) & 1, abort, p.err);
+      for (int n0 = n_lo; n0 < n_hi; n0 += nb, advance()) {
+        const int st = cst;
+        mbar_wait(&meta.full[st], cph, abort, p.err);
         const uint8_t *stage = ring + (size_t)st * cfg.stage_bytes;
         const int rows = min(nb, n_hi - n0);
-        float o[rpt][kNPG];   // per B row of this thread
+        // B vectors and y_in values to registers, then the stage goes back
+        uint4 bv[kVecsPerThread];
+#pragma unroll
+        for (int i = 0; i < kVecsPerThread; ++i) {
+          const int row = brow0 + i / cpt;
+          if (row < rows) bv[i] = *reinterpret_cast<const uint4 *>(stage + ((size_t)row * vr + bc0 + ((i + row) & (cpt - 1))) * 16);
+        }
+        float old[rpt][kNPG];
 #pragma unroll
         for (int k = 0; k < rpt; ++k)
 #pragma unroll
-          for (int q = 0; q < kNPG; ++q) o[k][q] = 0.f;
+          for (int q = 0; q < kNPG; ++q) {
+            const int row = brow0 + k;
+            old[k][q] = p.add_inputs && q < ng && row < rows && (tid & (tpr - 1)) == 0
+                            ? bf16_bits_to_float(reinterpret_cast<const uint16_t *>(stage + cfg.b_bytes + q * nb * 2)[row])
+                            : 0.f;
+          }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta.empty[st]);
+        f32x2 o2[rpt][kNPG];   // per B row of this thread
+#pragma unroll
+        for (int k = 0; k < rpt; ++k)
+#pragma unroll
+          for (int q = 0; q < kNPG; ++q) o2[k][q] = 0ull;
 #pragma unroll
         for (int i = 0; i < kVecsPerThread; ++i) {
           const int k = i / cpt;   // row of this thread (0 .. rpt-1)
           const int row = brow0 + k;
           if (row < rows) {
             const int cv = bc0 + ((i + row) & (cpt - 1));   // rotated vector of the row
-            const uint4 bv = *reinterpret_cast<const uint4 *>(stage + ((size_t)row * vr + cv) * 16);
+            f32x2 bf[4];
+            unpack_v(bv[i], bf);
 #pragma unroll
             for (int q = 0; q < kNPG; ++q)
-              if (q < ng) o[k][q] += dot8_bf16_f32(bv, tf + q * r + cv * 8);
+              if (q < ng) {
+                // t[q][8 cv .. 8 cv + 8) as four f32x2 (two 16-byte loads)
+                const ulonglong2 t01 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv * 8);
+                const ulonglong2 t23 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv * 8 + 4);
+                o2[k][q] = ffma2(bf[0], t01.x, o2[k][q]);
+                o2[k][q] = ffma2(bf[1], t01.y, o2[k][q]);
+                o2[k][q] = ffma2(bf[2], t23.x, o2[k][q]);
+                o2[k][q] = ffma2(bf[3], t23.y, o2[k][q]);
+              }
           }
         }
+        float o[rpt][kNPG];
+#pragma unroll
+        for (int k = 0; k < rpt; ++k)
+#pragma unroll
+          for (int q = 0; q < kNPG; ++q) o[k][q] = f2_sum(o2[k][q]);
         if (tpr > 1) {
 #pragma unroll
           for (int q = 0; q < kNPG; ++q)
@@ -475,17 +523,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (row < rows)
 #pragma unroll
               for (int q = 0; q < kNPG; ++q)
-                if (q < ng) {
-                  const float old =
-                      p.add_inputs
-                          ? bf16_bits_to_float(reinterpret_cast<const uint16_t *>(stage + cfg.b_bytes + q * nb * 2)[row])
-                          : 0.f;
-                  p.y[(size_t)fq[q] * p.ldy + col0 + n0 + row] = float_to_bf16_bits(o[k][q] * wq[q] + old);
-                }
+                if (q < ng) p.y[(size_t)fq[q] * p.ldy + col0 + n0 + row] = float_to_bf16_bits(o[k][q] * wq[q] + old[k][q]);
           }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&meta.empty[st]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&meta.dempty[d]);
@@ -498,84 +538,106 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int ng = min(ds.ng, kNPG);
       // every consumer thread takes the same decision (no thread may leave
       // the named barriers below to the others)
-      if (!named_barrier_and(1, kConsumers, ng > 0 && !*abort)) break;
-      const int b = item & 1;
-      // this CTA receives C partials of ng x r floats for the item
-      if (tid == 0) mbar_arrive_expect_tx(&meta.t_ready[b], (uint32_t)(C * ng * r * 4));
+      const bool more = named_barrier_and(1, kConsumers, ng > 0 && !*abort);
+      if (more) {
+        const int b = item & 1;
+        // this CTA receives C partials of ng x r floats for the item
+        if (tid == 0) mbar_arrive_expect_tx(&meta.t_ready[b], (uint32_t)(C * ng * r * 4));
 
-      // ---- shrink: this CTA's partial t over its K columns
-      float acc[kVecsPerThread][kNPG];
-#pragma unroll
-      for (int i = 0; i < kVecsPerThread; ++i)
-#pragma unroll
-        for (int q = 0; q < kNPG; ++q) acc[i][q] = 0.f;
-      for (int k0 = k_lo; k0 < k_hi; k0 += kc, ++it) {
-        const int st = it % NS;
-        mbar_wait(&meta.full[st], (it / NS) & 1, abort, p.err);
-        const uint8_t *stage = ring + (size_t)st * cfg.stage_bytes;
-        // this thread's column vector is the same in all its rows (va divides
-        // the consumer threads): its x pieces are read once per stage
-        if (cv_a < k_hi - k0) {
-          uint4 xv[kNPG];
-#pragma unroll
-          for (int q = 0; q < kNPG; ++q)
-            if (q < ng) xv[q] = *reinterpret_cast<const uint4 *>(stage + cfg.a_bytes + (q * kc + cv_a) * 2);
-          uint4 av[kVecsPerThread];
-#pragma unroll
-          for (int i = 0; i < kVecsPerThread; ++i)
-            if (i * kConsumers < r * va) av[i] = *reinterpret_cast<const uint4 *>(stage + (size_t)(i * kConsumers + tid) * 16);
-#pragma unroll
-          for (int i = 0; i < kVecsPerThread; ++i)
-            if (i * kConsumers < r * va)
-#pragma unroll
-              for (int q = 0; q < kNPG; ++q)
-                if (q < ng) acc[i][q] += dot8_bf16(av[i], xv[q]);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&meta.empty[st]);
-      }
-      // sum each row's partial over the va lanes that share it (va <= 32:
-      // consecutive lanes); the first of them keeps it
-#pragma unroll
-      for (int i = 0; i < kVecsPerThread; ++i)
-#pragma unroll
-        for (int q = 0; q < kNPG; ++q)
-          if (q < ng) {
-            float v = acc[i][q];
-#pragma unroll
-            for (int dd = va >> 1; dd > 0; dd >>= 1) v += __shfl_xor_sync(0xffffffffu, v, dd);
-            acc[i][q] = v;
-          }
-      if ((tid & (va - 1)) == 0) {
-#pragma unroll
-        for (int i = 0; i < kVecsPerThread; ++i) {
-          const int row = (i * kConsumers + tid) >> lg_va;
-          if (row < r)
-#pragma unroll
+        // ---- shrink: this CTA's partial t over its K columns
+        f32x2 acc2[kVecsPerThread][kNPG];
+  #pragma unroll
+        for (int i = 0; i < kVecsPerThread; ++i)
+  #pragma unroll
+          for (int q = 0; q < kNPG; ++q) acc2[i][q] = 0ull;   // two +0.0f
+        for (int k0 = k_lo; k0 < k_hi; k0 += kc, advance()) {
+          const int st = cst;
+          mbar_wait(&meta.full[st], cph, abort, p.err);
+          const uint8_t *stage = ring + (size_t)st * cfg.stage_bytes;
+          // The stage's vectors go to registers and the stage is handed back
+          // before any arithmetic, so that its next fill is in flight while
+          // this one is reduced.  This thread's column vector is the same in
+          // all its rows (va divides the consumer threads): its x pieces are
+          // read once per stage.
+          const bool live = cv_a < k_hi - k0;
+          uint4 xv[kNPG], av[kVecsPerThread];
+          if (live) {
+  #pragma unroll
             for (int q = 0; q < kNPG; ++q)
-              if (q < ng) stg[q * r + row] = acc[i][q];
+              if (q < ng) xv[q] = *reinterpret_cast<const uint4 *>(stage + cfg.a_bytes + (q * kc + cv_a) * 2);
+  #pragma unroll
+            for (int i = 0; i < kVecsPerThread; ++i)
+              if (i * kConsumers < r * va) av[i] = *reinterpret_cast<const uint4 *>(stage + (size_t)(i * kConsumers + tid) * 16);
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&meta.empty[st]);
+          if (live) {
+            f32x2 xf[kNPG][4];
+  #pragma unroll
+            for (int q = 0; q < kNPG; ++q)
+              if (q < ng) unpack_v(xv[q], xf[q]);
+  #pragma unroll
+            for (int i = 0; i < kVecsPerThread; ++i)
+              if (i * kConsumers < r * va) {
+                f32x2 af[4];
+                unpack_v(av[i], af);
+  #pragma unroll
+                for (int q = 0; q < kNPG; ++q)
+                  if (q < ng) {
+  #pragma unroll
+                    for (int h = 0; h < 4; ++h) acc2[i][q] = ffma2(af[h], xf[q][h], acc2[i][q]);
+                  }
+              }
+          }
         }
-      }
-      // every CTA is done with its buffer b (two items back) before this
-      // item's partials go into it
-      if (item >= 2 && tid == 0) mbar_wait_cluster(&meta.t_free[b], ((item >> 1) - 1) & 1, abort, p.err);
-      named_barrier(1, kConsumers);
-      {
-        const int nv4 = ng * r / 4;
-        const uint32_t src = smem_addr(rbuf + (size_t)(b * C + c) * kNPG * r);
-        const uint32_t bar = smem_addr(&meta.t_ready[b]);
-        for (int i = tid; i < C * nv4; i += kConsumers) {
-          const int dst = i / nv4, v = i - dst * nv4;
-          const float4 val = reinterpret_cast<const float4 *>(stg)[v];
-          st_async_v4(cluster_map(src + v * 16, dst), val, cluster_map(bar, dst));
+        // sum each row's partial over the va lanes that share it (va <= 32:
+        // consecutive lanes); the first of them keeps it
+        float acc[kVecsPerThread][kNPG];
+  #pragma unroll
+        for (int i = 0; i < kVecsPerThread; ++i)
+  #pragma unroll
+          for (int q = 0; q < kNPG; ++q) acc[i][q] = f2_sum(acc2[i][q]);
+  #pragma unroll
+        for (int i = 0; i < kVecsPerThread; ++i)
+  #pragma unroll
+          for (int q = 0; q < kNPG; ++q)
+            if (q < ng) {
+              float v = acc[i][q];
+  #pragma unroll
+              for (int dd = va >> 1; dd > 0; dd >>= 1) v += __shfl_xor_sync(0xffffffffu, v, dd);
+              acc[i][q] = v;
+            }
+        if ((tid & (va - 1)) == 0) {
+  #pragma unroll
+          for (int i = 0; i < kVecsPerThread; ++i) {
+            const int row = (i * kConsumers + tid) >> lg_va;
+            if (row < r)
+  #pragma unroll
+              for (int q = 0; q < kNPG; ++q)
+                if (q < ng) stg[q * r + row] = acc[i][q];
+          }
+        }
+        // every CTA is done with its buffer b (two items back) before this
+        // item's partials go into it
+        if (item >= 2 && tid == 0) mbar_wait_cluster(&meta.t_free[b], ((item >> 1) - 1) & 1, abort, p.err);
+        named_barrier(1, kConsumers);
+        {
+          const int nv4 = ng * r / 4;
+          const uint32_t src = smem_addr(rbuf + (size_t)(b * C + c) * kNPG * r);
+          const uint32_t bar = smem_addr(&meta.t_ready[b]);
+          for (int i = tid; i < C * nv4; i += kConsumers) {
+            const int dst = i / nv4, v = i - dst * nv4;
+            const float4 val = reinterpret_cast<const float4 *>(stg)[v];
+            st_async_v4(cluster_map(src + v * 16, dst), val, cluster_map(bar, dst));
+          }
         }
       }
       // the previous item's exchange has had this item's shrink to land
       if (have_prev) finish(pv_item);
+      if (!more) break;
       have_prev = true;
       pv_item = item;
     }
-    if (have_prev) finish(pv_item);
   }
   // no CTA leaves while a peer may still write into its shared memory or
   // arrive on its barriers
