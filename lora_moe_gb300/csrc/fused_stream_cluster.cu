@@ -61,7 +61,9 @@ constexpr int kMaxStages = 24;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxSlots = 128;              // listed slots the work list indexes
 constexpr int kStageVecs = 1024;            // 16-byte adapter vectors per ring stage (16 KB)
+constexpr int kRowsPerThread = 4;           // B rows per consumer thread and stage (one 8-column piece each)
 constexpr int kVecsPerThread = kStageVecs / kConsumers;
+static_assert(kRowsPerThread == kVecsPerThread, "a stage's B vectors are four per consumer thread");
 constexpr int kCtasPerSm = 2;               // two rings and 16 consumer warps per SM
 
 struct CsCfg {
@@ -141,6 +143,54 @@ __device__ __forceinline__ void unpack_v(const uint4 v, f32x2 (&f)[4]) {
   f[1] = bf2_to_f2(v.y);
   f[2] = bf2_to_f2(v.z);
   f[3] = bf2_to_f2(v.w);
+}
+
+// Row sums over a group of G consecutive lanes (G a power of two up to 32),
+// each lane holding partial sums of the same V rows.  While a lane holds more
+// than one row, a step with lane distance d hands half of its rows to the
+// partner and keeps the other half plus the partner's share of it; once one
+// row is left, the remaining steps are plain butterflies.  A lane ends with
+// rows_reduce_out() consecutive row sums, starting at row rows_reduce_base().
+template <int G, int V>
+__host__ __device__ constexpr int rows_reduce_out() {
+  return G >= V ? 1 : V / G;
+}
+template <int G, int V>
+__device__ __forceinline__ int rows_reduce_base(int lane) {
+  int base = 0, n = V;
+#pragma unroll
+  for (int d = G / 2; d >= 1; d >>= 1)
+    if (n > 1) {
+      n >>= 1;
+      if (lane & d) base += n;
+    }
+  return base;
+}
+// Of the lanes holding the same sums, the one that writes them.
+template <int G, int V>
+__device__ __forceinline__ bool rows_reduce_keeper(int lane) {
+  return G <= V || (lane & (G / V - 1)) == 0;
+}
+template <int G, int V>
+__device__ __forceinline__ void rows_reduce(float (&v)[V], int lane) {
+  int n = V;
+#pragma unroll
+  for (int d = G / 2; d >= 1; d >>= 1) {
+    if (n > 1) {
+      const int h = n >> 1;
+      const bool up = (lane & d) != 0;
+#pragma unroll
+      for (int k = 0; k < V / 2; ++k)
+        if (k < h) {
+          const float send = up ? v[k] : v[k + h];
+          const float keep = up ? v[k + h] : v[k];
+          v[k] = keep + __shfl_xor_sync(0xffffffffu, send, d);
+        }
+      n = h;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], d);
+    }
+  }
 }
 
 __device__ __forceinline__ int find_slot(const int *prefix, int nact, int item) {
@@ -397,17 +447,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ================================================= consumer warps
     // Shrink: thread tid owns the A vectors g = i * 256 + tid (i < 4) of a
     // stage: row g / va, column vector g % va; a warp reads 512 contiguous
-    // bytes per step.  Expand: thread tid owns the B vectors 4 tid .. 4 tid + 3
-    // (row-major, vr per row), read in an order rotated by the row so that the
-    // lanes of a quarter warp hit distinct banks.
+    // bytes per step.  Expand: thread tid owns column vector tid % vr of the
+    // four B rows 4 (tid / vr) .. + 3 (a quarter warp reads 128 contiguous
+    // bytes); the vr lanes of a row group then sum each row between them.
     constexpr int lg_vr = LG_VR, vr = 1 << LG_VR;
     constexpr int lg_va = kLgVa<LG_VR>, va = 1 << lg_va;
-    constexpr int cpt = vr < kVecsPerThread ? vr : kVecsPerThread;     // B vectors per row per thread
-    constexpr int rpt = kVecsPerThread / cpt;                             // B rows per thread
-    constexpr int tpr = vr > kVecsPerThread ? vr / kVecsPerThread : 1;   // threads per B row
+    constexpr int kOut = rows_reduce_out<vr, kRowsPerThread>();           // row sums a lane ends with
     const int cv_a = (tid & (va - 1)) * 8;                                // this thread's A column (elements)
-    const int brow0 = (kVecsPerThread * tid) >> lg_vr;                   // first B row of this thread
-    const int bc0 = (kVecsPerThread * tid) & (vr - 1);                   // its first vector in that row
+    const int cv_b = tid & (vr - 1);                                      // its B column vector
+    const int erow0 = (tid >> lg_vr) * kRowsPerThread;                    // its first B row in a stage
+    const int obase = rows_reduce_base<vr, kRowsPerThread>(lane);         // its first summed row (of erow0 ..)
+    const bool store_lane = rows_reduce_keeper<vr, kRowsPerThread>(lane); // it writes those rows
     float *rbuf = reinterpret_cast<float *>(smem + cfg.off_rbuf);
     float *tfull = reinterpret_cast<float *>(smem + cfg.off_tfull);
     float *stg = reinterpret_cast<float *>(smem + cfg.off_stg);
@@ -453,7 +503,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // this thread's y stores still in flight.
       if (tid == 0)
         for (int dst = 0; dst < C; ++dst) mbar_arrive_remote_relaxed(cluster_map(smem_addr(&meta.t_free[b]), dst));
-      // ---- expand: this CTA's output rows
+      // ---- expand: this CTA's output rows.  This thread's t columns are
+      // the same in every stage of the item: they stay in registers.
+      f32x2 tq[kNPG][4];
+#pragma unroll
+      for (int q = 0; q < kNPG; ++q) {
+        if (q < ng) {
+          const ulonglong2 t01 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8);
+          const ulonglong2 t23 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8 + 4);
+          tq[q][0] = t01.x;
+          tq[q][1] = t01.y;
+          tq[q][2] = t23.x;
+          tq[q][3] = t23.y;
+        } else {
+#pragma unroll
+          for (int h = 0; h < 4; ++h) tq[q][h] = 0ull;
+        }
+      }
       const int col0 = p.y_offset + s * N;
       for (int n0 = n_lo; n0 < n_hi; n0 += nb, advance()) {
         const int st = cst;
@@ -461,69 +527,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const uint8_t *stage = ring + (size_t)st * cfg.stage_bytes;
         const int rows = min(nb, n_hi - n0);
         // B vectors and y_in values to registers, then the stage goes back
-        uint4 bv[kVecsPerThread];
+        uint4 bv[kRowsPerThread];
 #pragma unroll
-        for (int i = 0; i < kVecsPerThread; ++i) {
-          const int row = brow0 + i / cpt;
-          if (row < rows) bv[i] = *reinterpret_cast<const uint4 *>(stage + ((size_t)row * vr + bc0 + ((i + row) & (cpt - 1))) * 16);
-        }
-        float old[rpt][kNPG];
+        for (int j = 0; j < kRowsPerThread; ++j)
+          if (erow0 + j < rows) bv[j] = *reinterpret_cast<const uint4 *>(stage + ((size_t)(erow0 + j) * vr + cv_b) * 16);
+        float old[kOut][kNPG];
 #pragma unroll
-        for (int k = 0; k < rpt; ++k)
+        for (int k = 0; k < kOut; ++k)
 #pragma unroll
           for (int q = 0; q < kNPG; ++q) {
-            const int row = brow0 + k;
-            old[k][q] = p.add_inputs && q < ng && row < rows && (tid & (tpr - 1)) == 0
+            const int row = erow0 + obase + k;
+            old[k][q] = p.add_inputs && store_lane && q < ng && row < rows
                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t *>(stage + cfg.b_bytes + q * nb * 2)[row])
                             : 0.f;
           }
         __syncwarp();
         if (lane == 0) mbar_arrive(&meta.empty[st]);
-        f32x2 o2[rpt][kNPG];   // per B row of this thread
+        // this thread's 8-column piece of each of its rows
+        float o[kNPG][kRowsPerThread];
 #pragma unroll
-        for (int k = 0; k < rpt; ++k)
+        for (int j = 0; j < kRowsPerThread; ++j) {
+          f32x2 bf[4];
+          unpack_v(erow0 + j < rows ? bv[j] : make_uint4(0u, 0u, 0u, 0u), bf);
 #pragma unroll
-          for (int q = 0; q < kNPG; ++q) o2[k][q] = 0ull;
-#pragma unroll
-        for (int i = 0; i < kVecsPerThread; ++i) {
-          const int k = i / cpt;   // row of this thread (0 .. rpt-1)
-          const int row = brow0 + k;
-          if (row < rows) {
-            const int cv = bc0 + ((i + row) & (cpt - 1));   // rotated vector of the row
-            f32x2 bf[4];
-            unpack_v(bv[i], bf);
-#pragma unroll
-            for (int q = 0; q < kNPG; ++q)
-              if (q < ng) {
-                // t[q][8 cv .. 8 cv + 8) as four f32x2 (two 16-byte loads)
-                const ulonglong2 t01 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv * 8);
-                const ulonglong2 t23 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv * 8 + 4);
-                o2[k][q] = ffma2(bf[0], t01.x, o2[k][q]);
-                o2[k][q] = ffma2(bf[1], t01.y, o2[k][q]);
-                o2[k][q] = ffma2(bf[2], t23.x, o2[k][q]);
-                o2[k][q] = ffma2(bf[3], t23.y, o2[k][q]);
-              }
+          for (int q = 0; q < kNPG; ++q) {
+            f32x2 acc = ffma2(bf[0], tq[q][0], 0ull);
+            acc = ffma2(bf[1], tq[q][1], acc);
+            acc = ffma2(bf[2], tq[q][2], acc);
+            acc = ffma2(bf[3], tq[q][3], acc);
+            o[q][j] = f2_sum(acc);
           }
         }
-        float o[rpt][kNPG];
+        // sum over the vr lanes of each row (ng is the same in every lane)
 #pragma unroll
-        for (int k = 0; k < rpt; ++k)
+        for (int q = 0; q < kNPG; ++q)
+          if (q < ng) rows_reduce<vr, kRowsPerThread>(o[q], lane);
+        if (store_lane) {
 #pragma unroll
-          for (int q = 0; q < kNPG; ++q) o[k][q] = f2_sum(o2[k][q]);
-        if (tpr > 1) {
-#pragma unroll
-          for (int q = 0; q < kNPG; ++q)
-            if (q < ng)
-              for (int dd = tpr >> 1; dd > 0; dd >>= 1) o[0][q] += __shfl_xor_sync(0xffffffffu, o[0][q], dd);
-        }
-        if ((tid & (tpr - 1)) == 0) {
-#pragma unroll
-          for (int k = 0; k < rpt; ++k) {
-            const int row = brow0 + k;
+          for (int k = 0; k < kOut; ++k) {
+            const int row = erow0 + obase + k;
             if (row < rows)
 #pragma unroll
               for (int q = 0; q < kNPG; ++q)
-                if (q < ng) p.y[(size_t)fq[q] * p.ldy + col0 + n0 + row] = float_to_bf16_bits(o[k][q] * wq[q] + old[k][q]);
+                if (q < ng) p.y[(size_t)fq[q] * p.ldy + col0 + n0 + row] = float_to_bf16_bits(o[q][k] * wq[q] + old[k][q]);
           }
         }
       }
