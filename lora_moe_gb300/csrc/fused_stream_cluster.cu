@@ -450,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // bytes per step.  Expand: thread tid owns column vector tid % vr of the
     // four B rows 4 (tid / vr) .. + 3 (a quarter warp reads 128 contiguous
     // bytes); the vr lanes of a row group then sum each row between them.
+    constexpr int NPG = NAIVE ? 1 : kNPG;   // pairs an item can hold (the naive assignment: one)
     constexpr int lg_vr = LG_VR, vr = 1 << LG_VR;
     constexpr int lg_va = kLgVa<LG_VR>, va = 1 << lg_va;
     constexpr int kOut = rows_reduce_out<vr, kRowsPerThread>();           // row sums a lane ends with
@@ -479,12 +480,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     auto finish = [&](uint32_t itm) {
       const int d = itm % kDesc, b = itm & 1;
       const Desc &ds = meta.desc[d];
-      const int ng = min(ds.ng, kNPG);
+      const int ng = min(ds.ng, NPG);
       const int s = ds.s;
-      float wq[kNPG];
-      int fq[kNPG];
+      float wq[NPG];
+      int fq[NPG];
 #pragma unroll
-      for (int q = 0; q < kNPG; ++q) {
+      for (int q = 0; q < NPG; ++q) {
         wq[q] = q < ng ? ds.w[q] : 0.f;
         fq[q] = q < ng ? ds.f[q] : 0;
       }
@@ -503,22 +504,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // this thread's y stores still in flight.
       if (tid == 0)
         for (int dst = 0; dst < C; ++dst) mbar_arrive_remote_relaxed(cluster_map(smem_addr(&meta.t_free[b]), dst));
-      // ---- expand: this CTA's output rows.  This thread's t columns are
-      // the same in every stage of the item: they stay in registers.
-      f32x2 tq[kNPG][4];
+      // ---- expand: this CTA's output rows.  This thread's t columns (8 per
+      // pair) are the same in every stage of the item: they stay in registers.
+      f32x2 tq[NPG][4];
 #pragma unroll
-      for (int q = 0; q < kNPG; ++q) {
-        if (q < ng) {
-          const ulonglong2 t01 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8);
-          const ulonglong2 t23 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8 + 4);
-          tq[q][0] = t01.x;
-          tq[q][1] = t01.y;
-          tq[q][2] = t23.x;
-          tq[q][3] = t23.y;
-        } else {
-#pragma unroll
-          for (int h = 0; h < 4; ++h) tq[q][h] = 0ull;
-        }
+      for (int q = 0; q < NPG; ++q) {
+        const ulonglong2 t01 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8);
+        const ulonglong2 t23 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8 + 4);
+        tq[q][0] = t01.x;
+        tq[q][1] = t01.y;
+        tq[q][2] = t23.x;
+        tq[q][3] = t23.y;
       }
       const int col0 = p.y_offset + s * N;
       for (int n0 = n_lo; n0 < n_hi; n0 += nb, advance()) {
@@ -531,11 +527,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int j = 0; j < kRowsPerThread; ++j)
           if (erow0 + j < rows) bv[j] = *reinterpret_cast<const uint4 *>(stage + ((size_t)(erow0 + j) * vr + cv_b) * 16);
-        float old[kOut][kNPG];
+        float old[kOut][NPG];
 #pragma unroll
         for (int k = 0; k < kOut; ++k)
 #pragma unroll
-          for (int q = 0; q < kNPG; ++q) {
+          for (int q = 0; q < NPG; ++q) {
             const int row = erow0 + obase + k;
             old[k][q] = p.add_inputs && store_lane && q < ng && row < rows
                             ? bf16_bits_to_float(reinterpret_cast<const uint16_t *>(stage + cfg.b_bytes + q * nb * 2)[row])
@@ -544,13 +540,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
         if (lane == 0) mbar_arrive(&meta.empty[st]);
         // this thread's 8-column piece of each of its rows
-        float o[kNPG][kRowsPerThread];
+        float o[NPG][kRowsPerThread];
 #pragma unroll
         for (int j = 0; j < kRowsPerThread; ++j) {
           f32x2 bf[4];
           unpack_v(erow0 + j < rows ? bv[j] : make_uint4(0u, 0u, 0u, 0u), bf);
 #pragma unroll
-          for (int q = 0; q < kNPG; ++q) {
+          for (int q = 0; q < NPG; ++q) {
             f32x2 acc = ffma2(bf[0], tq[q][0], 0ull);
             acc = ffma2(bf[1], tq[q][1], acc);
             acc = ffma2(bf[2], tq[q][2], acc);
@@ -560,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         // sum over the vr lanes of each row (ng is the same in every lane)
 #pragma unroll
-        for (int q = 0; q < kNPG; ++q)
+        for (int q = 0; q < NPG; ++q)
           if (q < ng) rows_reduce<vr, kRowsPerThread>(o[q], lane);
         if (store_lane) {
 #pragma unroll
@@ -568,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int row = erow0 + obase + k;
             if (row < rows)
 #pragma unroll
-              for (int q = 0; q < kNPG; ++q)
+              for (int q = 0; q < NPG; ++q)
                 if (q < ng) p.y[(size_t)fq[q] * p.ldy + col0 + n0 + row] = float_to_bf16_bits(o[q][k] * wq[q] + old[k][q]);
           }
         }
@@ -581,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int d = item % kDesc;
       mbar_wait(&meta.dfull[d], (item / kDesc) & 1, abort, p.err);
       const Desc &ds = meta.desc[d];
-      const int ng = min(ds.ng, kNPG);
+      const int ng = min(ds.ng, NPG);
       // every consumer thread takes the same decision (no thread may leave
       // the named barriers below to the others)
       const bool more = named_barrier_and(1, kConsumers, ng > 0 && !*abort);
@@ -591,11 +587,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (tid == 0) mbar_arrive_expect_tx(&meta.t_ready[b], (uint32_t)(C * ng * r * 4));
 
         // ---- shrink: this CTA's partial t over its K columns
-        f32x2 acc2[kVecsPerThread][kNPG];
-  #pragma unroll
+        float acc[kVecsPerThread][NPG];
+#pragma unroll
         for (int i = 0; i < kVecsPerThread; ++i)
-  #pragma unroll
-          for (int q = 0; q < kNPG; ++q) acc2[i][q] = 0ull;   // two +0.0f
+#pragma unroll
+          for (int q = 0; q < NPG; ++q) acc[i][q] = 0.f;
         for (int k0 = k_lo; k0 < k_hi; k0 += kc, advance()) {
           const int st = cst;
           mbar_wait(&meta.full[st], cph, abort, p.err);
@@ -606,60 +602,57 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           // all its rows (va divides the consumer threads): its x pieces are
           // read once per stage.
           const bool live = cv_a < k_hi - k0;
-          uint4 xv[kNPG], av[kVecsPerThread];
+          uint4 xv[NPG], av[kVecsPerThread];
           if (live) {
-  #pragma unroll
-            for (int q = 0; q < kNPG; ++q)
+#pragma unroll
+            for (int q = 0; q < NPG; ++q)
               if (q < ng) xv[q] = *reinterpret_cast<const uint4 *>(stage + cfg.a_bytes + (q * kc + cv_a) * 2);
-  #pragma unroll
+#pragma unroll
             for (int i = 0; i < kVecsPerThread; ++i)
               if (i * kConsumers < r * va) av[i] = *reinterpret_cast<const uint4 *>(stage + (size_t)(i * kConsumers + tid) * 16);
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&meta.empty[st]);
           if (live) {
-            f32x2 xf[kNPG][4];
-  #pragma unroll
-            for (int q = 0; q < kNPG; ++q)
-              if (q < ng) unpack_v(xv[q], xf[q]);
-  #pragma unroll
-            for (int i = 0; i < kVecsPerThread; ++i)
-              if (i * kConsumers < r * va) {
-                f32x2 af[4];
-                unpack_v(av[i], af);
-  #pragma unroll
-                for (int q = 0; q < kNPG; ++q)
-                  if (q < ng) {
-  #pragma unroll
-                    for (int h = 0; h < 4; ++h) acc2[i][q] = ffma2(af[h], xf[q][h], acc2[i][q]);
+            // pair by pair (an item mostly holds one), so that only one x
+            // piece is unpacked at a time
+#pragma unroll
+            for (int q = 0; q < NPG; ++q)
+              if (q < ng) {
+                f32x2 xf[4];
+                unpack_v(xv[q], xf);
+#pragma unroll
+                for (int i = 0; i < kVecsPerThread; ++i)
+                  if (i * kConsumers < r * va) {
+                    f32x2 af[4];
+                    unpack_v(av[i], af);
+                    f32x2 d2 = ffma2(af[0], xf[0], 0ull);
+#pragma unroll
+                    for (int h = 1; h < 4; ++h) d2 = ffma2(af[h], xf[h], d2);
+                    acc[i][q] += f2_sum(d2);
                   }
               }
           }
         }
         // sum each row's partial over the va lanes that share it (va <= 32:
         // consecutive lanes); the first of them keeps it
-        float acc[kVecsPerThread][kNPG];
-  #pragma unroll
+#pragma unroll
         for (int i = 0; i < kVecsPerThread; ++i)
-  #pragma unroll
-          for (int q = 0; q < kNPG; ++q) acc[i][q] = f2_sum(acc2[i][q]);
-  #pragma unroll
-        for (int i = 0; i < kVecsPerThread; ++i)
-  #pragma unroll
-          for (int q = 0; q < kNPG; ++q)
+#pragma unroll
+          for (int q = 0; q < NPG; ++q)
             if (q < ng) {
               float v = acc[i][q];
-  #pragma unroll
+#pragma unroll
               for (int dd = va >> 1; dd > 0; dd >>= 1) v += __shfl_xor_sync(0xffffffffu, v, dd);
               acc[i][q] = v;
             }
         if ((tid & (va - 1)) == 0) {
-  #pragma unroll
+#pragma unroll
           for (int i = 0; i < kVecsPerThread; ++i) {
             const int row = (i * kConsumers + tid) >> lg_va;
             if (row < r)
-  #pragma unroll
-              for (int q = 0; q < kNPG; ++q)
+#pragma unroll
+              for (int q = 0; q < NPG; ++q)
                 if (q < ng) stg[q * r + row] = acc[i][q];
           }
         }
