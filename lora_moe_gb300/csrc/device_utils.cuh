@@ -164,6 +164,12 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t rbar) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
 }
 
+// Plain 32-bit store into a peer's (or this CTA's) shared memory at
+// shared::cluster address `raddr`; visible to the peer after a cluster barrier.
+__device__ __forceinline__ void st_cluster_u32(uint32_t raddr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(raddr), "r"(v) : "memory");
+}
+
 // Asynchronous 16-byte store into a peer's (or this CTA's) shared memory at
 // shared::cluster address `raddr`; its bytes are counted as completed
 // transactions on the mbarrier at shared::cluster address `rbar` of the same CTA.

@@ -31,7 +31,7 @@
 //     with st.async (completion counted on the peer's mbarrier), sum the C
 //     partials in rank order (deterministic) and expand their N rows.  t never
 //     leaves shared memory or registers.
-//   * a unit with more than kNPG real pairs is applied kNPG pairs at a time
+//   * a unit with more than NPG real pairs is applied NPG pairs at a time
 //     (its adapters re-streamed, from L2).
 // Every wait is bounded.
 #include <cooperative_groups.h>
@@ -55,11 +55,13 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kProducerWarps = 2;           // stage it is issued by producer warp it % 2
 constexpr int kThreads = kConsumers + kProducerWarps * 32;
-constexpr int kNPG = 2;                     // pairs per work item
+constexpr int kNPG = 2;                     // most pairs a work item holds (NPG: 1 or kNPG)
 constexpr int kDesc = 8;                    // work-item descriptors in flight
 constexpr int kMaxStages = 24;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxSlots = 128;              // listed slots the work list indexes
+constexpr int kListCap = 32;                // work items a cluster takes from the balanced list
+constexpr int kScanPerThread = 4;           // blocks a thread counts when the list is built
 constexpr int kStageVecs = 1024;            // 16-byte adapter vectors per ring stage (16 KB)
 constexpr int kRowsPerThread = 4;           // B rows per consumer thread and stage (one 8-column piece each)
 constexpr int kVecsPerThread = kStageVecs / kConsumers;
@@ -74,11 +76,12 @@ struct CsCfg {
   int lg_vr;         // log2(r / 8): vectors per B row
   int stages;
   int stage_bytes;
-  int a_bytes;       // r * kc * 2: the A box; kNPG x pieces of kc * 2 bytes follow
-  int b_bytes;       // nb * r * 2: the B rows; kNPG y_in pieces of nb * 2 bytes follow
-  int off_rbuf;      // fp32 [2][C][kNPG][r]: partial t received from each CTA
-  int off_tfull;     // fp32 [2][kNPG][r]: summed t
-  int off_stg;       // fp32 [kNPG][r]: this CTA's partial t
+  int npg;           // pairs per work item (the kernel's NPG)
+  int a_bytes;       // r * kc * 2: the A box; npg x pieces of kc * 2 bytes follow
+  int b_bytes;       // nb * r * 2: the B rows; npg y_in pieces of nb * 2 bytes follow
+  int off_rbuf;      // fp32 [2][C][npg][r]: partial t received from each CTA
+  int off_tfull;     // fp32 [2][npg][r]: summed t
+  int off_stg;       // fp32 [npg][r]: this CTA's partial t
   int off_meta;
   int smem_bytes;
   int k_lo[kMaxCluster], k_hi[kMaxCluster], n_lo[kMaxCluster], n_hi[kMaxCluster];
@@ -104,6 +107,9 @@ struct CsMeta {
   int prefix[kMaxSlots + 1];
   int lids[kMaxSlots];                  // lora_ids (naive block assignment)
   int pf[kProducerWarps][128];          // each producer: the current block's real pairs
+  int scan[kThreads / 32][kNPG];        // per-warp item counts by pair count (list building)
+  int list[kListCap];                   // this cluster's work items: (block, group, slice)
+  int nlist;                            // their number, or -1: no list (every unit in turn)
   int abort;
 };
 
@@ -143,6 +149,23 @@ __device__ __forceinline__ void unpack_v(const uint4 v, f32x2 (&f)[4]) {
   f[1] = bf2_to_f2(v.y);
   f[2] = bf2_to_f2(v.z);
   f[3] = bf2_to_f2(v.w);
+}
+
+// c + sum_i a[i] * b[i] over one 16-byte vector of bf16 pairs: mixed
+// precision FMAs (bf16 operands, exact products, fp32 accumulation and
+// rounding), so neither operand is widened first.
+__device__ __forceinline__ float dot8_bf16_acc(const uint4 a, const uint4 b, float c) {
+  const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+        "mov.b32 {al, ah}, %1;\n\t"
+        "mov.b32 {bl, bh}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
+        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
+        : "+f"(c)
+        : "r"(wa[i]), "r"(wb[i]));
+  return c;
 }
 
 // Row sums over a group of G consecutive lanes (G a power of two up to 32),
@@ -202,13 +225,124 @@ __device__ __forceinline__ int find_slot(const int *prefix, int nact, int item) 
   return lo;
 }
 
+// The sorted blocks' work as a balanced list, built by all threads of one CTA
+// per cluster from the same inputs (so every cluster sees the same order).  Block b
+// holds n_b real pairs, applied NPG at a time: n_b / NPG items of NPG pairs
+// and one of n_b % NPG pairs (if any), each once per slice.  The items are
+// ordered by their pair count (most first), then by block, group and slice,
+// and dealt out to the G clusters in a snake (0 .. G-1, G-1 .. 0, ...): each
+// cluster gets floor or ceil(items / G) of them, one per round, and the
+// heavy ones are spread.  Entry `round` of cluster g's list encodes
+// (block << 8) | (group << 2) | slice.  No list (nlist = -1) when the blocks
+// outnumber what the threads count in one pass or a share exceeds kListCap;
+// the units are then taken in turn.
+template <int NPG>
+__device__ void build_item_list(CsMeta &meta, const FusedArgs &p, int nact, int S, int P, int G, int g, int tid) {
+  const int lane = tid & 31, warp = tid >> 5;
+  const int nblk = meta.prefix[nact];
+  if (nblk > kThreads * kScanPerThread) {
+    if (tid == 0) meta.nlist = -1;
+    __syncthreads();
+    return;
+  }
+  // this thread's blocks: a contiguous run, so that the scan follows block order
+  const int per = (nblk + kThreads - 1) / kThreads;
+  const int b0 = tid * per;
+  int nbk[kScanPerThread];
+  int cnt[NPG];   // this thread's items with k + 1 pairs
+#pragma unroll
+  for (int k = 0; k < NPG; ++k) cnt[k] = 0;
+#pragma unroll
+  for (int i = 0; i < kScanPerThread; ++i) {
+    nbk[i] = 0;
+    const int b = b0 + i;
+    if (i < per && b < nblk) {
+      const int z = find_slot(meta.prefix, nact, b);
+      const int l = __ldg(p.lora_ids + z);
+      const int32_t *ids =
+          p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + (size_t)(b - meta.prefix[z]) * p.block_size;
+      int n = 0;
+      if ((reinterpret_cast<uintptr_t>(ids) & 15) == 0 && (p.block_size & 3) == 0) {
+#pragma unroll 4
+        for (int k = 0; k < p.block_size; k += 4) {
+          const int4 v = __ldg(reinterpret_cast<const int4 *>(ids + k));
+          n += (v.x >= 0 && v.x < P) + (v.y >= 0 && v.y < P) + (v.z >= 0 && v.z < P) + (v.w >= 0 && v.w < P);
+        }
+      } else {
+#pragma unroll 8
+        for (int k = 0; k < p.block_size; ++k) {
+          const int f = __ldg(ids + k);
+          n += (f >= 0 && f < P) ? 1 : 0;
+        }
+      }
+      nbk[i] = n;
+      cnt[NPG - 1] += n / NPG;
+      if (n % NPG) cnt[n % NPG - 1] += 1;
+    }
+  }
+  // exclusive scan of the counts over the threads (block order)
+  int incl[NPG];
+#pragma unroll
+  for (int k = 0; k < NPG; ++k) {
+    int v = cnt[k];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, v, d);
+      if (lane >= d) v += o;
+    }
+    incl[k] = v;
+    if (lane == 31) meta.scan[warp][k] = v;
+  }
+  __syncthreads();
+  int run[NPG], off[NPG];
+  long long items = 0;
+#pragma unroll
+  for (int k = NPG - 1; k >= 0; --k) {
+    int before = 0, all = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const int v = meta.scan[w][k];
+      if (w < warp) before += v;
+      all += v;
+    }
+    run[k] = before + incl[k] - cnt[k];   // rank of this thread's first item with k + 1 pairs
+    off[k] = (int)items;                   // items with more pairs come first
+    items += all;
+  }
+  const long long total = items * S;
+  const long long rounds = (total + G - 1) / G;
+  if (rounds > kListCap) {
+    if (tid == 0) meta.nlist = -1;
+    __syncthreads();
+    return;
+  }
+  // this cluster's count: one per full round, and one in the last partial
+  // round when the snake's direction there covers it
+  const long long full = total / G, rest = total - full * G;
+  const bool in_last = rest > 0 && ((full & 1) ? g >= G - rest : g < rest);
+  if (tid == 0) meta.nlist = (int)(full + (in_last ? 1 : 0));
+#pragma unroll
+  for (int i = 0; i < kScanPerThread; ++i) {
+    const int n = nbk[i], b = b0 + i;
+    const int groups = n / NPG + (n % NPG ? 1 : 0);
+    for (int j = 0; j < groups; ++j) {
+      const int k = (j < n / NPG ? NPG : n % NPG) - 1;
+      const long long idx0 = (long long)(off[k] + run[k]++) * S;
+      for (int s = 0; s < S; ++s) {
+        const long long idx = idx0 + s, round = idx / G, pos = idx - round * G;
+        if (((round & 1) ? G - 1 - pos : pos) == g) meta.list[round] = (b << 8) | (j << 2) | s;
+      }
+    }
+  }
+  __syncthreads();
+}
+
 // log2 of the 16-byte vectors per A box row: the box has min(256, 8192 / r)
 // columns (at most kStageVecs vectors), r = 8 << LG_VR.
 template <int LG_VR>
 constexpr int kLgVa = (7 - LG_VR) < 5 ? (7 - LG_VR) : 5;
 
 // LG_VR = log2(rank / 8): the rank (8 .. 128) fixes every per-thread loop.
-template <bool NAIVE, int LG_VR>
+template <bool NAIVE, int LG_VR, int NPG>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     fused_cluster_stream_kernel(const __grid_constant__ CsMaps maps, const FusedArgs p, const CsCfg cfg) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -280,6 +414,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     units = (long long)P * S;
   }
   const int G = gridDim.x / C, g = blockIdx.x / C;
+  if (!NAIVE) {
+    // the cluster's CTAs take the same items: rank 0 builds the list and
+    // writes it into the others' shared memory
+    if (c == 0) {
+      build_item_list<NPG>(meta, p, nact, S, P, G, g, tid);
+      for (int i = tid; i < (kListCap + 1) * (C - 1); i += kThreads) {
+        const int dst = 1 + i / (kListCap + 1), k = i - (dst - 1) * (kListCap + 1);
+        int *src = k < kListCap ? &meta.list[k] : &meta.nlist;
+        st_cluster_u32(cluster_map(smem_addr(src), dst), (uint32_t)*src);
+      }
+    }
+    if (C > 1) {
+      cluster_arrive_release();
+      cluster_wait();
+    }
+  }
   const int k_lo = cfg.k_lo[c], k_hi = cfg.k_hi[c], n_lo = cfg.n_lo[c], n_hi = cfg.n_hi[c];
 
   if (warp >= kConsumerWarps) {
@@ -294,8 +444,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const bool lead = lane == 0;
     // the previous item (its B stages follow the current item's A stages)
     bool have_prev = false;
-    int pv_s = 0, pv_le = 0, pv_ng = 0, pv_f[kNPG];
-    auto issue_b = [&](int s_, int le_, int ng_, const int (&f_)[kNPG]) {
+    int pv_s = 0, pv_le = 0, pv_ng = 0, pv_f[NPG];
+    auto issue_b = [&](int s_, int le_, int ng_, const int (&f_)[NPG]) {
       if (!lead) return;
       const uint16_t *Bm = slice_b(p, s_) + (size_t)le_ * N * r;
       const int col0 = p.y_offset + s_ * N;
@@ -311,14 +461,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         bulk_g2s(stage, Bm + (size_t)n0 * r, bb, &meta.full[st]);
         if (p.add_inputs) {
 #pragma unroll
-          for (int q = 0; q < kNPG; ++q)
+          for (int q = 0; q < NPG; ++q)
             if (q < ng_)
               bulk_g2s(stage + cfg.b_bytes + q * nb * 2, p.y + (size_t)f_[q] * p.ldy + col0 + n0, yb, &meta.full[st]);
         }
       }
     };
-    for (long long u = g; u < units; u += G) {
+    // the units in turn (u = g, g + G, ...), or this cluster's entries of the
+    // balanced list (one group of one block's pairs each)
+    const int nlist = NAIVE ? -1 : meta.nlist;
+    const long long nwork = nlist >= 0 ? nlist : (units > g ? (units - 1 - g) / G + 1 : 0);
+    for (long long w = 0; w < nwork; ++w) {
       if (__shfl_sync(0xffffffffu, *abort, 0)) break;
+      long long u = g + w * G;
+      int jsel = -1;   // the one group this entry takes (-1: all of the unit's)
+      if (nlist >= 0) {
+        const int code = meta.list[w];
+        jsel = (code >> 2) & 63;
+        u = (long long)(code >> 8) * S + (code & 3);
+      }
       int s, le, np = 0;
       if (!NAIVE) {
         const int gb = (int)(u / S);
@@ -359,8 +520,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
         np = 1;
       }
-      for (int g0 = 0; g0 < np; g0 += kNPG) {
-        const int ng = min(kNPG, np - g0);
+      const int g_first = jsel < 0 ? 0 : jsel * NPG, g_end = jsel < 0 ? np : min(np, g_first + NPG);
+      for (int g0 = g_first; g0 < g_end; g0 += NPG) {
+        const int ng = min(NPG, np - g0);
         int fq = -1, xq = 0;
         if (lane < ng) {
           fq = pf[g0 + lane];
@@ -384,9 +546,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           if (lead) mbar_arrive(&meta.dfull[d]);
         }
         // the pairs' rows, in every lane (lane q < ng holds pair q)
-        int xr[kNPG], fr[kNPG];
+        int xr[NPG], fr[NPG];
 #pragma unroll
-        for (int q = 0; q < kNPG; ++q) {
+        for (int q = 0; q < NPG; ++q) {
           xr[q] = __shfl_sync(0xffffffffu, xq, q);
           fr[q] = __shfl_sync(0xffffffffu, fq, q);
         }
@@ -404,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             mbar_arrive_expect_tx(&meta.full[st], (uint32_t)cfg.a_bytes + ng * xb);
             tma_load_3d(stage, &maps.a[s], k0, 0, le, &meta.full[st]);
 #pragma unroll
-            for (int q = 0; q < kNPG; ++q)
+            for (int q = 0; q < NPG; ++q)
               if (q < ng) bulk_g2s(stage + cfg.a_bytes + q * kc * 2, p.x + (size_t)xr[q] * K + k0, xb, &meta.full[st]);
           }
         }
@@ -415,7 +577,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         pv_le = le;
         pv_ng = ng;
 #pragma unroll
-        for (int q = 0; q < kNPG; ++q) pv_f[q] = fr[q];
+        for (int q = 0; q < NPG; ++q) pv_f[q] = fr[q];
         ++item;
         __syncwarp();
       }
@@ -450,7 +612,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // bytes per step.  Expand: thread tid owns column vector tid % vr of the
     // four B rows 4 (tid / vr) .. + 3 (a quarter warp reads 128 contiguous
     // bytes); the vr lanes of a row group then sum each row between them.
-    constexpr int NPG = NAIVE ? 1 : kNPG;   // pairs an item can hold (the naive assignment: one)
     constexpr int lg_vr = LG_VR, vr = 1 << LG_VR;
     constexpr int lg_va = kLgVa<LG_VR>, va = 1 << lg_va;
     constexpr int kOut = rows_reduce_out<vr, kRowsPerThread>();           // row sums a lane ends with
@@ -491,10 +652,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       }
       if (tid == 0) mbar_wait_cluster(&meta.t_ready[b], (itm >> 1) & 1, abort, p.err);
       named_barrier(1, kConsumers);
-      float *tf = tfull + (size_t)b * kNPG * r;
+      float *tf = tfull + (size_t)b * NPG * r;
       for (int i = tid; i < ng * r; i += kConsumers) {
         float sum = 0.f;
-        for (int q = 0; q < C; ++q) sum += rbuf[(size_t)(b * C + q) * kNPG * r + i];
+        for (int q = 0; q < C; ++q) sum += rbuf[(size_t)(b * C + q) * NPG * r + i];
         tf[i] = sum;
       }
       named_barrier(1, kConsumers);
@@ -504,18 +665,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // this thread's y stores still in flight.
       if (tid == 0)
         for (int dst = 0; dst < C; ++dst) mbar_arrive_remote_relaxed(cluster_map(smem_addr(&meta.t_free[b]), dst));
-      // ---- expand: this CTA's output rows.  This thread's t columns (8 per
-      // pair) are the same in every stage of the item: they stay in registers.
-      f32x2 tq[NPG][4];
-#pragma unroll
-      for (int q = 0; q < NPG; ++q) {
-        const ulonglong2 t01 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8);
-        const ulonglong2 t23 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8 + 4);
-        tq[q][0] = t01.x;
-        tq[q][1] = t01.y;
-        tq[q][2] = t23.x;
-        tq[q][3] = t23.y;
-      }
+      // ---- expand: this CTA's output rows
       const int col0 = p.y_offset + s * N;
       for (int n0 = n_lo; n0 < n_hi; n0 += nb, advance()) {
         const int st = cst;
@@ -526,7 +676,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         uint4 bv[kRowsPerThread];
 #pragma unroll
         for (int j = 0; j < kRowsPerThread; ++j)
-          if (erow0 + j < rows) bv[j] = *reinterpret_cast<const uint4 *>(stage + ((size_t)(erow0 + j) * vr + cv_b) * 16);
+          bv[j] = erow0 + j < rows ? *reinterpret_cast<const uint4 *>(stage + ((size_t)(erow0 + j) * vr + cv_b) * 16)
+                                   : make_uint4(0u, 0u, 0u, 0u);
         float old[kOut][NPG];
 #pragma unroll
         for (int k = 0; k < kOut; ++k)
@@ -539,35 +690,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           }
         __syncwarp();
         if (lane == 0) mbar_arrive(&meta.empty[st]);
-        // this thread's 8-column piece of each of its rows
-        float o[NPG][kRowsPerThread];
-#pragma unroll
-        for (int j = 0; j < kRowsPerThread; ++j) {
-          f32x2 bf[4];
-          unpack_v(erow0 + j < rows ? bv[j] : make_uint4(0u, 0u, 0u, 0u), bf);
-#pragma unroll
-          for (int q = 0; q < NPG; ++q) {
-            f32x2 acc = ffma2(bf[0], tq[q][0], 0ull);
-            acc = ffma2(bf[1], tq[q][1], acc);
-            acc = ffma2(bf[2], tq[q][2], acc);
-            acc = ffma2(bf[3], tq[q][3], acc);
-            o[q][j] = f2_sum(acc);
-          }
-        }
-        // sum over the vr lanes of each row (ng is the same in every lane)
+        // pair by pair: this thread's 8 t columns (the same in every stage of
+        // the item), its 8-column piece of each of its rows, the sums over the
+        // vr lanes of each row (ng is the same in every lane), the stores.
+        // (Widening each B vector once for all pairs would hold their t
+        // columns and sums at once: more registers than a thread has here.)
 #pragma unroll
         for (int q = 0; q < NPG; ++q)
-          if (q < ng) rows_reduce<vr, kRowsPerThread>(o[q], lane);
-        if (store_lane) {
+          if (q < ng) {
+            const ulonglong2 t01 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8);
+            const ulonglong2 t23 = *reinterpret_cast<const ulonglong2 *>(tf + q * r + cv_b * 8 + 4);
+            float o[kRowsPerThread];
 #pragma unroll
-          for (int k = 0; k < kOut; ++k) {
-            const int row = erow0 + obase + k;
-            if (row < rows)
+            for (int j = 0; j < kRowsPerThread; ++j) {
+              f32x2 bf[4];
+              unpack_v(bv[j], bf);
+              f32x2 acc = ffma2(bf[0], t01.x, 0ull);
+              acc = ffma2(bf[1], t01.y, acc);
+              acc = ffma2(bf[2], t23.x, acc);
+              acc = ffma2(bf[3], t23.y, acc);
+              o[j] = f2_sum(acc);
+            }
+            rows_reduce<vr, kRowsPerThread>(o, lane);
+            if (store_lane) {
+              uint16_t *yq = p.y + (size_t)fq[q] * p.ldy + col0 + n0;
 #pragma unroll
-              for (int q = 0; q < NPG; ++q)
-                if (q < ng) p.y[(size_t)fq[q] * p.ldy + col0 + n0 + row] = float_to_bf16_bits(o[q][k] * wq[q] + old[k][q]);
+              for (int k = 0; k < kOut; ++k) {
+                const int row = erow0 + obase + k;
+                if (row < rows) yq[row] = float_to_bf16_bits(o[k] * wq[q] + old[k][q]);
+              }
+            }
           }
-        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&meta.dempty[d]);
@@ -614,23 +767,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           __syncwarp();
           if (lane == 0) mbar_arrive(&meta.empty[st]);
           if (live) {
-            // pair by pair (an item mostly holds one), so that only one x
-            // piece is unpacked at a time
 #pragma unroll
             for (int q = 0; q < NPG; ++q)
               if (q < ng) {
-                f32x2 xf[4];
-                unpack_v(xv[q], xf);
 #pragma unroll
                 for (int i = 0; i < kVecsPerThread; ++i)
-                  if (i * kConsumers < r * va) {
-                    f32x2 af[4];
-                    unpack_v(av[i], af);
-                    f32x2 d2 = ffma2(af[0], xf[0], 0ull);
-#pragma unroll
-                    for (int h = 1; h < 4; ++h) d2 = ffma2(af[h], xf[h], d2);
-                    acc[i][q] += f2_sum(d2);
-                  }
+                  if (i * kConsumers < r * va) acc[i][q] = dot8_bf16_acc(av[i], xv[q], acc[i][q]);
               }
           }
         }
@@ -662,7 +804,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         named_barrier(1, kConsumers);
         {
           const int nv4 = ng * r / 4;
-          const uint32_t src = smem_addr(rbuf + (size_t)(b * C + c) * kNPG * r);
+          const uint32_t src = smem_addr(rbuf + (size_t)(b * C + c) * NPG * r);
           const uint32_t bar = smem_addr(&meta.t_ready[b]);
           for (int i = tid; i < C * nv4; i += kConsumers) {
             const int dst = i / nv4, v = i - dst * nv4;
@@ -690,11 +832,13 @@ int ilog2(int v) {
   return l;
 }
 
-// Geometry and shared-memory layout for C CTAs per cluster.
-bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, CsCfg *cfg) {
+// Geometry and shared-memory layout for C CTAs per cluster and npg pairs per
+// work item.
+bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, int npg, CsCfg *cfg) {
   const int r = f.rank;
   if (r < 8 || r > 128 || (r & (r - 1)) != 0) return false;   // ranks 8, 16, 32, 64, 128
   cfg->C = C;
+  cfg->npg = npg;
   int kc = 256;
   while (r * kc > kStageVecs * 8) kc >>= 1;   // the A box holds at most kStageVecs vectors
   cfg->kc = kc;
@@ -703,8 +847,8 @@ bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, CsCfg *cfg) {
   cfg->lg_vr = ilog2(r / 8);
   cfg->a_bytes = r * kc * 2;
   cfg->b_bytes = cfg->nb * r * 2;
-  const int st_a = cfg->a_bytes + kNPG * kc * 2, st_b = cfg->b_bytes + kNPG * cfg->nb * 2;
-  cfg->stage_bytes = (std::max(st_a, st_b) + 1023) / 1024 * 1024;
+  const int st_a = cfg->a_bytes + npg * kc * 2, st_b = cfg->b_bytes + npg * cfg->nb * 2;
+  cfg->stage_bytes = (std::max(st_a, st_b) + 127) / 128 * 128;   // TMA destinations: 128-byte aligned
   const int k8 = f.K / 8, n8 = f.N / 8;
   for (int i = 0; i < kMaxCluster; ++i) {
     const int cc = i < C ? i : C - 1;
@@ -713,7 +857,7 @@ bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, CsCfg *cfg) {
     cfg->n_lo[i] = (cc * n8 / C) * 8;
     cfg->n_hi[i] = ((cc + 1) * n8 / C) * 8;
   }
-  const int rbuf = 2 * C * kNPG * r * 4, tfull = 2 * kNPG * r * 4, stg = kNPG * r * 4;
+  const int rbuf = 2 * C * npg * r * 4, tfull = 2 * npg * r * 4, stg = npg * r * 4;
   const int fixed = rbuf + tfull + stg + ((int)sizeof(CsMeta) + 127) / 128 * 128;
   // kCtasPerSm CTAs share an SM's 228 KB (each CTA also reserves 1 KB)
   const int budget = std::min((int)dev.max_smem_optin, 228 * 1024 / kCtasPerSm - 1024);
@@ -729,7 +873,7 @@ bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, CsCfg *cfg) {
   return cfg->smem_bytes <= budget;
 }
 
-template <bool NAIVE, int LG_VR>
+template <bool NAIVE, int LG_VR, int NPG>
 int resident_clusters(const CsCfg &cfg, const DeviceInfo &dev) {
   struct Entry {
     int device, C, smem, clusters;
@@ -741,7 +885,7 @@ int resident_clusters(const CsCfg &cfg, const DeviceInfo &dev) {
   for (int i = 0; i < n; ++i)
     if (cache[i].device == dev.device && cache[i].C == cfg.C && cache[i].smem == cfg.smem_bytes)
       return cache[i].clusters;
-  const void *fn = (const void *)fused_cluster_stream_kernel<NAIVE, LG_VR>;
+  const void *fn = (const void *)fused_cluster_stream_kernel<NAIVE, LG_VR, NPG>;
   int clusters = 0;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes) == cudaSuccess) {
     cudaLaunchConfig_t lc = {};
@@ -763,45 +907,44 @@ int resident_clusters(const CsCfg &cfg, const DeviceInfo &dev) {
   return clusters;
 }
 
-// Units the call may have (host bound): blocks x slices, or pairs x slices.
-long long unit_bound(const FusedArgs &f, bool naive) {
-  if (naive) return (long long)f.M * f.topk * f.num_slices;
+// Work items the call may have (host bound): pairs x slices (the naive
+// assignment, or blocks applied one pair at a time), else blocks x slices.
+long long unit_bound(const FusedArgs &f, bool naive, int npg) {
+  if (naive || npg == 1) return (long long)f.M * f.topk * f.num_slices;
   return fused_block_bound(f.M, f.topk, f.num_experts, f.num_active_loras, f.block_size) * f.num_slices;
 }
 
-// The cluster size, its configuration and grid (clusters).  Measured on the
-// gpt-oss-shaped w2 decode (rank 64, K = N = 2880) and the Qwen3-shaped w13
-// decode: blocks of the align output run best split over 4 CTAs (the K and N
-// halves of 2 CTAs stream too long a share per CTA, 8-CTA exchanges cost more
-// than they balance), pairs of the naive assignment (one unit each, more units
-// than CTA slots) unsplit.  Smaller clusters are taken when K or N has too few
-// 8-element chunks.  resident(C) gives the clusters of size C that fit at once.
+// Pairs per work item and cluster size.  Measured on the gpt-oss-shaped w2
+// decode (rank 64, K = N = 2880) and the Qwen3-shaped w13 decode.  Pairs of
+// the naive assignment: one per item, clusters of one CTA.  Blocks of the
+// align output when the pairs are no more than the (LoRA, expert) pairs
+// (decode: mostly one pair per block): one pair per item, from a balanced
+// list, clusters of one CTA -- a block's second pair re-reads its adapters,
+// mostly from L2, rather than doubling the arithmetic of one CTA (gpt-oss
+// w2 decode: 31 us against 40 us).  Fuller blocks: up to kNPG pairs per item,
+// split over 4 CTAs (K and N halves of 2 CTAs stream too long a share per
+// CTA; 8-CTA exchanges cost more than they balance).  Smaller clusters are
+// taken when K or N has too few 8-element chunks.  resident(cfg) gives the
+// clusters of that shape that fit at once.
 template <typename ResidentFn>
 int choose(const FusedArgs &f, const DeviceInfo &dev, bool naive, ResidentFn resident, CsCfg *out, long long *grid) {
-  const long long units = unit_bound(f, naive);
-  int want = naive ? 1 : 4;
+  const bool single = naive || (long long)f.M * f.topk <= (long long)f.num_experts * f.num_active_loras;
+  const int npg = single ? 1 : kNPG;
+  int want = single ? 1 : 4;
   while (want > 1 && (f.K / 8 < want || f.N / 8 < want)) want >>= 1;
   for (int C = want; C >= 1; C >>= 1) {
     CsCfg cfg;
-    if (!layout(f, dev, C, &cfg)) continue;
+    if (!layout(f, dev, C, npg, &cfg)) continue;
     const int clusters = resident(cfg);
     *out = cfg;
-    *grid = std::max(1LL, std::min<long long>(units, clusters));
+    *grid = std::max(1LL, std::min<long long>(unit_bound(f, naive, npg), clusters));
     return 0;
   }
   return MOE_LORA_ERR_UNSUPPORTED;
 }
 
-template <bool NAIVE, int LG_VR>
-int launch_cs(const FusedArgs &f, cudaStream_t stream) {
-  DeviceInfo dev;
-  if (int st = current_device_info(&dev)) return st;
-  CsCfg cfg;
-  long long G = 0;
-  if (int st = choose(f, dev, NAIVE, [&](const CsCfg &c) { return resident_clusters<NAIVE, LG_VR>(c, dev); }, &cfg,
-                      &G))
-    return st;
-  if (unit_bound(f, NAIVE) <= 0) return 0;
+template <bool NAIVE, int LG_VR, int NPG>
+int launch_with(const FusedArgs &f, const CsCfg &cfg, long long G, cudaStream_t stream) {
   CsMaps maps;
   const uint64_t LE = (uint64_t)f.max_loras * f.num_experts;
   for (int s = 0; s < kMaxSlices; ++s) {
@@ -810,7 +953,7 @@ int launch_cs(const FusedArgs &f, cudaStream_t stream) {
                                    (uint32_t)f.rank, CU_TENSOR_MAP_SWIZZLE_NONE))
       return st;
   }
-  const void *fn = (const void *)fused_cluster_stream_kernel<NAIVE, LG_VR>;
+  const void *fn = (const void *)fused_cluster_stream_kernel<NAIVE, LG_VR, NPG>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, cfg.smem_bytes) != cudaSuccess)
     return MOE_LORA_ERR_LAUNCH;
   cudaLaunchConfig_t lc = {};
@@ -830,9 +973,25 @@ int launch_cs(const FusedArgs &f, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  return cudaLaunchKernelEx(&lc, fused_cluster_stream_kernel<NAIVE, LG_VR>, maps, f, cfg) == cudaSuccess
+  return cudaLaunchKernelEx(&lc, fused_cluster_stream_kernel<NAIVE, LG_VR, NPG>, maps, f, cfg) == cudaSuccess
              ? 0
              : MOE_LORA_ERR_LAUNCH;
+}
+
+template <bool NAIVE, int LG_VR>
+int launch_cs(const FusedArgs &f, cudaStream_t stream) {
+  DeviceInfo dev;
+  if (int st = current_device_info(&dev)) return st;
+  CsCfg cfg;
+  long long G = 0;
+  auto resident = [&](const CsCfg &c) {
+    if constexpr (NAIVE) return resident_clusters<NAIVE, LG_VR, 1>(c, dev);
+    else return c.npg == 1 ? resident_clusters<NAIVE, LG_VR, 1>(c, dev) : resident_clusters<NAIVE, LG_VR, kNPG>(c, dev);
+  };
+  if (int st = choose(f, dev, NAIVE, resident, &cfg, &G)) return st;
+  if (unit_bound(f, NAIVE, cfg.npg) <= 0) return 0;
+  if constexpr (NAIVE) return launch_with<NAIVE, LG_VR, 1>(f, cfg, G, stream);
+  else return cfg.npg == 1 ? launch_with<NAIVE, LG_VR, 1>(f, cfg, G, stream) : launch_with<NAIVE, LG_VR, kNPG>(f, cfg, G, stream);
 }
 
 template <bool NAIVE>
@@ -879,7 +1038,7 @@ int plan_fused_cluster_stream(const FusedArgs &f, const DeviceInfo &dev, bool na
   out->t_bufs = cfg.nb;   // (fields reused: A box columns, B rows per stage)
   out->tmem_cols = 0;
   out->cluster = cfg.C;
-  out->pairs_per_group = kNPG;
+  out->pairs_per_group = cfg.npg;
   return 0;
 }
 

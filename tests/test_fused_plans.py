@@ -21,7 +21,7 @@ def plan_of(w, **kw):
 # tensor-core kernel; (kernel, CTAs per cluster, pairs per group) for the
 # CUDA-core kernels.  These are the plans the measured numbers were taken with.
 PINNED = {
-    "decode_gptoss_w2": (B.PATH_CUDA_CORE_STREAM, 4, 2),
+    "decode_gptoss_w2": (B.PATH_CUDA_CORE_STREAM, 1, 1),
     "prefill_mixtral_w13": (B.PATH_TCGEN05, 10, 4, 6, 1, 256),
     "large_e_nact1": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
     "large_e_nact8": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
@@ -77,7 +77,11 @@ def test_plan_invariants(path):
             assert p["grid"] % C == 0 and 1 <= p["grid"] <= 2 * 152, p
             assert p["s_sh"] >= 4 and p["threads"] == 320, p
             assert p["smem_bytes"] <= 113 * 1024, p
-            assert p["pairs_per_group"] == 2, p
+            # one pair per item where the pairs are no more than the (LoRA,
+            # expert) pairs, else two over clusters of up to 4 CTAs
+            single = M * topk <= E * 2   # nact = 2 in these plans
+            assert p["pairs_per_group"] == (1 if single else 2), p
+            assert C == 1 if single else C <= 4, p
             assert r * p["s_ex"] * 2 <= 16384 and p["t_bufs"] * r * 2 <= 16384, p   # A box, B rows per stage
         else:
             assert 1 <= p["cluster"] <= 16 and p["pairs_per_group"] in (1, 2, 8)
@@ -157,13 +161,17 @@ def test_plan_rejects_what_the_kernel_cannot_run():
 
 
 def test_cluster_stream_plan_gptoss_decode():
-    """The cluster streaming kernel on the gpt-oss decode shape: clusters of
-    4 CTAs, two CTAs of 10 warps per SM, each with a ring of six 16.5 KB stages (A
-    boxes of 64 ranks x 128 columns, B pieces of 128 rows x 64 ranks, each with
-    the pairs' x or y_in pieces)."""
+    """The cluster streaming kernel on the gpt-oss decode shape: 256 pairs
+    against 768 (LoRA, expert) pairs, so one pair per work item on CTAs of
+    their own (one per pair), two CTAs of 10 warps per SM, each with a ring of
+    six 16.25 KB stages (A boxes of 64 ranks x 128 columns, B pieces of 128
+    rows x 64 ranks, each with the pair's x or y_in piece).  A prefill batch of
+    the same shape takes two pairs per item over clusters of 4 CTAs."""
     p = B.fused_plan(64, 4, 128, 2880, 2880, 64, 6, 16, path=B.PATH_CUDA_CORE_STREAM, **GB300)
     assert p["kernel"] == B.PATH_CUDA_CORE_STREAM
-    assert p["cluster"] in (1, 2, 4, 8) and p["grid"] % p["cluster"] == 0 and p["grid"] <= 2 * 152
-    assert p["cluster"] == 4 and p["s_sh"] == 6 and p["threads"] == 320  # cluster, ring stages, threads
+    assert p["cluster"] == 1 and p["pairs_per_group"] == 1 and p["grid"] == 256
+    assert p["s_sh"] == 6 and p["threads"] == 320                        # ring stages, threads
     assert p["s_ex"] == 128 and p["t_bufs"] == 128                      # A columns, B rows per stage
     assert p["smem_bytes"] <= 113 * 1024                                # two CTAs share an SM
+    q = B.fused_plan(2048, 8, 128, 2880, 2880, 64, 6, 16, path=B.PATH_CUDA_CORE_STREAM, **GB300)
+    assert q["cluster"] == 4 and q["pairs_per_group"] == 2 and q["grid"] == 304
