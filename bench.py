@@ -140,7 +140,7 @@ def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weigh
 NCU_TRAFFIC = {
     ("decode_qwen3_w13", "fused_cuda_core_kernel"): 5573632,      # fused_cuda_core_decode_qwen3_w13.md
     ("decode_gptoss_w2", "fused_tcgen05_kernel"): 170909184,      # fused_tcgen05_decode_gptoss_w2.md
-    ("decode_gptoss_w2", "fused_cluster_stream_kernel"): 155535104,  # fused_cluster_stream_decode_gptoss_w2.md
+    ("decode_gptoss_w2", "fused_cluster_stream_kernel"): 155517696,  # fused_cluster_stream_decode_gptoss_w2.md
     ("large_e_l1", "fused_tcgen05_kernel"): 1080333056,           # fused_tcgen05_large_e_l1.md
     # the same active work as large_e_l1 (the inactive slots are never read)
     ("large_e_nact1", "fused_tcgen05_kernel"): 1080333056,        # fused_tcgen05_large_e_l1.md
