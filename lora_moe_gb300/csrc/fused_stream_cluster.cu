@@ -105,7 +105,7 @@ struct CsMeta {
   uint64_t t_ready[2], t_free[2];
   Desc desc[kDesc];
   int prefix[kMaxSlots + 1];
-  int lids[kMaxSlots];                  // lora_ids (naive block assignment)
+  int lids[kMaxSlots];                  // lora_ids (the naive assignment: -1 where disabled)
   int pf[kProducerWarps][128];          // each producer: the current block's real pairs
   int scan[kThreads / 32][kNPG];        // per-warp item counts by pair count (list building)
   int list[kListCap];                   // this cluster's work items: (block, group, slice)
@@ -258,7 +258,7 @@ __device__ void build_item_list(CsMeta &meta, const FusedArgs &p, int nact, int 
     const int b = b0 + i;
     if (i < per && b < nblk) {
       const int z = find_slot(meta.prefix, nact, b);
-      const int l = __ldg(p.lora_ids + z);
+      const int l = meta.lids[z];
       const int32_t *ids =
           p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + (size_t)(b - meta.prefix[z]) * p.block_size;
       int n = 0;
@@ -381,17 +381,42 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   wait_for_prior_grid();   // align outputs (and every other input) are read from here on
   long long units;
   if (!NAIVE) {
-    // blocks per listed slot and their prefix sum
-    for (int z = tid; z < nact; z += blockDim.x) {
-      const int l = __ldg(p.lora_ids + z);
+    // blocks per listed slot and their prefix sum; the slots' LoRA ids.  With
+    // at most 2 x 128 LoRAs, every LoRA's block count is read beside lora_ids
+    // (one round trip, not two), staged in the producers' pair lists.
+    int *nbl = &meta.pf[0][0];
+    const bool staged = p.max_loras <= kProducerWarps * 128;
+    if (staged) {
+      for (int l = tid; l < p.max_loras; l += blockDim.x) {
+        int nb_l = -1;   // -1: disabled
+        if (!p.adapter_enabled || __ldg(p.adapter_enabled + l) != 0)
+          nb_l = max(0, min(__ldg(p.num_tokens_post_padded + l) / p.block_size, p.max_num_m_blocks));
+        nbl[l] = nb_l;
+      }
+    }
+    int lz[(kMaxSlots + kThreads - 1) / kThreads];
+#pragma unroll
+    for (int i = 0; i < (kMaxSlots + kThreads - 1) / kThreads; ++i) {
+      const int z = tid + i * kThreads;
+      lz[i] = z < nact ? __ldg(p.lora_ids + z) : 0;
+    }
+    if (staged) __syncthreads();
+#pragma unroll
+    for (int i = 0; i < (kMaxSlots + kThreads - 1) / kThreads; ++i) {
+      const int z = tid + i * kThreads;
+      if (z >= nact) continue;
+      const int l = lz[i];
       int nb_z = 0;
       if (l < 0 || l >= p.max_loras) {
         if (blockIdx.x == 0) flag_error(p.err, MOE_LORA_DEVERR_LORA_ID);
+      } else if (staged) {
+        nb_z = max(0, nbl[l]);
       } else if (!p.adapter_enabled || __ldg(p.adapter_enabled + l) != 0) {
         nb_z = __ldg(p.num_tokens_post_padded + l) / p.block_size;
         nb_z = max(0, min(nb_z, p.max_num_m_blocks));
       }
       meta.prefix[z + 1] = nb_z;
+      meta.lids[z] = l;   // a slot with blocks has a valid id
     }
     __syncthreads();
     if (tid == 0) {
@@ -485,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int gb = (int)(u / S);
         s = (int)(u - (long long)gb * S);
         const int z = find_slot(meta.prefix, nact, gb);
-        const int l = __ldg(p.lora_ids + z);
+        const int l = meta.lids[z];
         const int b = gb - meta.prefix[z];
         const int e = __ldg(p.expert_ids + (size_t)l * p.max_num_m_blocks + b);
         if (e < 0 || e >= E) {
