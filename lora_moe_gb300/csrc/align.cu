@@ -83,15 +83,16 @@ __device__ __forceinline__ void warp_count(const AlignArgs &a, int l, int lo, in
   }
 }
 
-// Second walk: tab[e] holds this warp's next position in segment e.
+// Second walk: tab[e] + seg[e] (seg may be null) is this warp's next position
+// in segment e.
 __device__ __forceinline__ void warp_scatter(const AlignArgs &a, int l, int lo, int hi, int *tab,
-                                             int32_t *sorted, int lane) {
+                                             const int *seg, int32_t *sorted, int lane) {
   const unsigned lower = (1u << lane) - 1u;
   for (int base = lo; base < hi; base += 32) {
     const int f = base + lane;
     const int e = (f < hi) ? pair_expert(a, f, l, false) : -1;
     const unsigned peers = __match_any_sync(0xffffffffu, e);
-    const int pos = (e >= 0) ? tab[e] + __popc(peers & lower) : 0;
+    const int pos = (e >= 0) ? tab[e] + (seg ? seg[e] : 0) + __popc(peers & lower) : 0;
     __syncwarp();
     if (e >= 0) {
       sorted[pos] = f;
@@ -130,6 +131,53 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
   return excl;
 }
 
+// n ints from p (16-byte aligned) set to zero by the whole CTA.
+__device__ __forceinline__ void zero_ints(int *p, int n) {
+  const int n4 = n / 4;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) reinterpret_cast<int4 *>(p)[i] = make_int4(0, 0, 0, 0);
+  for (int i = n4 * 4 + threadIdx.x; i < n; i += blockDim.x) p[i] = 0;
+}
+
+// Column scan of a W x E table of per-warp counts (row w = warp w): every
+// entry becomes the count of the rows above it in its column, and cnt[e]
+// the column total.  One thread per column (consecutive columns: no bank
+// conflicts), its rows read eight at a time so that the loads of a batch are
+// in flight together.  Called by every thread of the CTA, with a barrier
+// before (the table complete) and after (the scan visible).
+__device__ __forceinline__ void column_scan(int *tab, int W, int E, int *cnt) {
+  const int e = threadIdx.x;
+  if (e >= E) return;
+  int run = 0, w = 0;
+  for (; w + 8 <= W; w += 8) {
+    int v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = tab[(w + i) * E + e];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      tab[(w + i) * E + e] = run;
+      run += v[i];
+    }
+  }
+  for (; w < W; ++w) {
+    const int v = tab[w * E + e];
+    tab[w * E + e] = run;
+    run += v;
+  }
+  cnt[e] = run;
+}
+
+// Padding sentinels and block labels of the segment of expert e (n real
+// pairs from offset o, padded to a block multiple), by one thread.
+__device__ __forceinline__ void write_padding(const AlignArgs &a, int l, int e, int n, int o) {
+  const int bs = a.block_size;
+  const int padded = (n + bs - 1) / bs * bs;
+  int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
+  int32_t *experts = a.expert_ids + (size_t)l * a.max_num_m_blocks;
+  const int sentinel = a.M * a.topk;
+  for (int i = o + n; i < o + padded; ++i) sorted[i] = sentinel;
+  for (int b = o / bs; b < (o + padded) / bs; ++b) experts[b] = e;
+}
+
 // Given per-expert counts cnt[e] (e < E, one per thread), compute segment
 // offsets off[0..E], write num_tokens_post_padded[l], the padding sentinels and
 // expert_ids.  Returns false (uniformly) when the result exceeds the caller's
@@ -151,14 +199,7 @@ __device__ bool write_segments(const AlignArgs &a, int l, const int *cnt, int *o
     return false;
   }
   if (tid == 0) a.num_tokens_post_padded[l] = total;
-  int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
-  int32_t *experts = a.expert_ids + (size_t)l * a.max_num_m_blocks;
-  const int sentinel = a.M * a.topk;
-  if (tid < E)
-    for (int i = excl + c; i < excl + padded; ++i) sorted[i] = sentinel;
-  // each expert's thread labels the blocks of its own segment
-  if (tid < E)
-    for (int b = excl / bs; b < (excl + padded) / bs; ++b) experts[b] = tid;
+  if (tid < E) write_padding(a, l, tid, c, excl);
   return true;
 }
 
@@ -212,8 +253,8 @@ __device__ __forceinline__ void warp_count_cached(const AlignArgs &a, int l, int
   }
 }
 
-__device__ __forceinline__ void warp_scatter_cached(int lo, int hi, int *tab, int32_t *sorted, int lane,
-                                                    const int (&ec)[kCache]) {
+__device__ __forceinline__ void warp_scatter_cached(int lo, int hi, int *tab, const int *seg, int32_t *sorted,
+                                                    int lane, const int (&ec)[kCache]) {
   const unsigned lower = (1u << lane) - 1u;
 #pragma unroll
   for (int it = 0; it < kCache; ++it) {
@@ -221,7 +262,7 @@ __device__ __forceinline__ void warp_scatter_cached(int lo, int hi, int *tab, in
     if (base < hi) {
       const int e = ec[it];
       const unsigned peers = __match_any_sync(0xffffffffu, e);
-      const int pos = (e >= 0) ? tab[e] + __popc(peers & lower) : 0;
+      const int pos = (e >= 0) ? tab[e] + seg[e] + __popc(peers & lower) : 0;
       __syncwarp();
       if (e >= 0) {
         sorted[pos] = base + lane;
@@ -261,7 +302,7 @@ __global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const Align
   const int l = slot_lora(a, blockIdx.x, tid == 0);
   if (l < 0) return;
 
-  for (int i = tid; i < W * E; i += blockDim.x) tab[i] = 0;
+  zero_ints(tab, W * E);
   __syncthreads();
 
   int *mine = tab + (warp < W ? warp : 0) * E;
@@ -273,25 +314,15 @@ __global__ void __launch_bounds__(kSmemThreads, 1) align_smem_kernel(const Align
   __syncthreads();
 
   // Column scan: each warp's starting position relative to its segment.
-  if (tid < E) {
-    int run = 0;
-    for (int w = 0; w < W; ++w) {
-      const int t = tab[w * E + tid];
-      tab[w * E + tid] = run;
-      run += t;
-    }
-    cnt[tid] = run;
-  }
+  column_scan(tab, W, E, cnt);
   __syncthreads();
   if (!write_segments(a, l, cnt, off, warp_sums)) return;
-  if (tid < E)
-    for (int w = 0; w < W; ++w) tab[w * E + tid] += off[tid];
-  __syncthreads();
 
+  // a warp's position in segment e: its column-scan entry + the segment's offset
   if (warp < W) {
     int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
-    if (cached) warp_scatter_cached(lo, hi, mine, sorted, lane, ec);
-    else warp_scatter(a, l, lo, hi, mine, sorted, lane);
+    if (cached) warp_scatter_cached(lo, hi, mine, off, sorted, lane, ec);
+    else warp_scatter(a, l, lo, hi, mine, off, sorted, lane);
   }
 }
 
@@ -389,7 +420,7 @@ __global__ void __launch_bounds__(kGlobalThreads) align_global_scatter_kernel(co
   __syncwarp();
   const int P = a.M * a.topk;
   const int lo = min(P, gw * g.pairs_per_warp), hi = min(P, lo + g.pairs_per_warp);
-  warp_scatter(a, l, lo, hi, mine, a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded, lane);
+  warp_scatter(a, l, lo, hi, mine, nullptr, a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded, lane);
 }
 
 // ----------------------------------------------------- cluster variant
@@ -414,10 +445,11 @@ __global__ void __launch_bounds__(kClusterAlignThreads, 1) align_cluster_kernel(
   cg::cluster_group cluster = cg::this_cluster();
   const int c = (int)cluster.block_rank();
   const int z = blockIdx.x / CA;
-  int *tab = smem;                                    // [W][E] per-warp counters, then cursors
+  int *tab = smem;                                    // [W][E] per-warp counters, then column-scanned
   int *cnt = tab + kClusterAlignWarps * E;            // [E] this CTA's counts (read by peers)
-  int *before = cnt + E;                              // [E] pairs of lower-ranked CTAs
-  int *off = before + E;                              // [E + 1]
+  int *before = cnt + E;                              // [E] pairs of lower-ranked CTAs, then scatter bases
+  int *tot = before + E;                              // [E] the slot's counts
+  int *off = tot + E;                                 // [E + 1]
   int *warp_sums = off + E + 1;                       // [32]
 
   asm volatile("griddepcontrol.launch_dependents;");
@@ -433,7 +465,7 @@ __global__ void __launch_bounds__(kClusterAlignThreads, 1) align_cluster_kernel(
   const int l = slot_lora(a, z, tid == 0 && c == 0);   // the same for every CTA of the cluster
   if (l < 0) return;                                    // (the whole cluster returns)
 
-  for (int i = tid; i < kClusterAlignWarps * E; i += blockDim.x) tab[i] = 0;
+  zero_ints(tab, kClusterAlignWarps * E);
   __syncthreads();
   int *mine = tab + warp * E;
   int ec[kCache];
@@ -441,15 +473,7 @@ __global__ void __launch_bounds__(kClusterAlignThreads, 1) align_cluster_kernel(
   else warp_count(a, l, lo, hi, mine, lane);
   __syncthreads();
   // column scan over this CTA's warps
-  if (tid < E) {
-    int run = 0;
-    for (int w = 0; w < kClusterAlignWarps; ++w) {
-      const int t = tab[w * E + tid];
-      tab[w * E + tid] = run;
-      run += t;
-    }
-    cnt[tid] = run;
-  }
+  column_scan(tab, kClusterAlignWarps, E, cnt);
   // every CTA's counts are complete before any CTA reads them
   cluster_arrive_release();
   cluster_wait();
@@ -461,43 +485,43 @@ __global__ void __launch_bounds__(kClusterAlignThreads, 1) align_cluster_kernel(
       if (q < c) below += v;
     }
     before[tid] = below;
-    off[tid] = total;   // the slot's count, turned into offsets below
+    tot[tid] = total;
   }
-  // no CTA reads a peer's counts after this: each may go on (and exit) freely
+  // This CTA reads no peer's counts after this.  The matching wait is at the
+  // end: no CTA exits while a peer may still read its counts.
   cluster_arrive_relaxed();
-  cluster_wait();
+  __syncthreads();
+  bool ok;
   {
-    const int n_e = tid < E ? off[tid] : 0;
+    const int n_e = tid < E ? tot[tid] : 0;
     const int padded = (n_e + a.block_size - 1) / a.block_size * a.block_size;
     int total;
     const int excl = block_exclusive_scan(padded, warp_sums, &total);
-    __syncthreads();
-    if (tid < E) off[tid] = excl;
+    if (tid < E) {
+      off[tid] = excl;
+      before[tid] += excl;   // this CTA's first position in segment tid
+    }
     if (tid == 0) off[E] = total;
     __syncthreads();
-    if (total > a.max_num_tokens_padded || total / a.block_size > a.max_num_m_blocks) {
+    ok = total <= a.max_num_tokens_padded && total / a.block_size <= a.max_num_m_blocks;
+    if (!ok) {
       if (tid == 0 && c == 0) {
         flag_error(a.err, MOE_LORA_DEVERR_CAPACITY);
         a.num_tokens_post_padded[l] = 0;
       }
-      return;
-    }
-    if (tid == 0 && c == 0) a.num_tokens_post_padded[l] = total;
-    if (tid < E && tid % CA == c) {
-      int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
-      int32_t *experts = a.expert_ids + (size_t)l * a.max_num_m_blocks;
-      const int sentinel = a.M * a.topk;
-      for (int i = excl + n_e; i < excl + padded; ++i) sorted[i] = sentinel;
-      for (int b = excl / a.block_size; b < (excl + padded) / a.block_size; ++b) experts[b] = tid;
+    } else {
+      if (tid == 0 && c == 0) a.num_tokens_post_padded[l] = total;
+      // experts e = c, c + CA, ...: sentinels and block labels by this CTA
+      if (tid < E && tid % CA == c) write_padding(a, l, tid, n_e, excl);
     }
   }
-  // each warp's first position in every segment
-  if (tid < E)
-    for (int w = 0; w < kClusterAlignWarps; ++w) tab[w * E + tid] += off[tid] + before[tid];
-  __syncthreads();
-  int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
-  if (cached) warp_scatter_cached(lo, hi, mine, sorted, lane, ec);
-  else warp_scatter(a, l, lo, hi, mine, sorted, lane);
+  if (ok) {
+    // a warp's position in segment e: its column-scan entry + this CTA's base
+    int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
+    if (cached) warp_scatter_cached(lo, hi, mine, before, sorted, lane, ec);
+    else warp_scatter(a, l, lo, hi, mine, before, sorted, lane);
+  }
+  cluster_wait();
 }
 
 int set_smem_limit(const void *fn, size_t bytes) {
@@ -551,13 +575,13 @@ int align_cluster_size(int M, int topk) {
 }
 
 bool align_cluster_fits(int E) {
-  const size_t bytes = ((size_t)kClusterAlignWarps * E + 3 * (size_t)E + 1 + 32) * sizeof(int);
+  const size_t bytes = ((size_t)kClusterAlignWarps * E + 4 * (size_t)E + 1 + 32) * sizeof(int);
   return bytes <= 200 * 1024;
 }
 
 int launch_align_cluster(const AlignArgs &a, cudaStream_t stream) {
   const int CA = align_cluster_size(a.M, a.topk);
-  const size_t bytes = ((size_t)kClusterAlignWarps * a.num_experts + 3 * (size_t)a.num_experts + 1 + 32) * sizeof(int);
+  const size_t bytes = ((size_t)kClusterAlignWarps * a.num_experts + 4 * (size_t)a.num_experts + 1 + 32) * sizeof(int);
   if (cudaFuncSetAttribute((const void *)align_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)bytes) != cudaSuccess)
     return MOE_LORA_ERR_LAUNCH;
