@@ -178,6 +178,24 @@ __device__ __forceinline__ void write_padding(const AlignArgs &a, int l, int e, 
   for (int b = o / bs; b < (o + padded) / bs; ++b) experts[b] = e;
 }
 
+// The same for experts e = e0, e0 + step, ... (counts n[e], offsets off[e]),
+// a warp per expert, its lanes one slot or block each: for CTAs with many
+// warps and few experts each.
+__device__ __forceinline__ void write_padding_warps(const AlignArgs &a, int l, const int *n, const int *off, int e0,
+                                                    int step) {
+  const int E = a.num_experts, bs = a.block_size;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  int32_t *sorted = a.sorted_token_ids + (size_t)l * a.max_num_tokens_padded;
+  int32_t *experts = a.expert_ids + (size_t)l * a.max_num_m_blocks;
+  const int sentinel = a.M * a.topk;
+  for (int e = e0 + warp * step; e < E; e += nwarps * step) {
+    const int c = n[e], o = off[e];
+    const int padded = (c + bs - 1) / bs * bs;
+    for (int i = c + lane; i < padded; i += 32) sorted[o + i] = sentinel;
+    for (int b = lane; b < padded / bs; b += 32) experts[o / bs + b] = e;
+  }
+}
+
 // Given per-expert counts cnt[e] (e < E, one per thread), compute segment
 // offsets off[0..E], write num_tokens_post_padded[l], the padding sentinels and
 // expert_ids.  Returns false (uniformly) when the result exceeds the caller's
@@ -512,7 +530,7 @@ __global__ void __launch_bounds__(kClusterAlignThreads, 1) align_cluster_kernel(
     } else {
       if (tid == 0 && c == 0) a.num_tokens_post_padded[l] = total;
       // experts e = c, c + CA, ...: sentinels and block labels by this CTA
-      if (tid < E && tid % CA == c) write_padding(a, l, tid, n_e, excl);
+      write_padding_warps(a, l, tot, off, c, CA);
     }
   }
   if (ok) {
@@ -564,9 +582,11 @@ int launch_align_smem(const AlignArgs &a, cudaStream_t stream) {
 }
 
 int align_cluster_size(int M, int topk) {
-  // about 4096 pairs (128 per warp, kept in registers between the walks) per CTA
+  // about 2048 pairs (64 per warp, kept in registers between the walks) per
+  // CTA, at most 8 CTAs (larger clusters could not all be placed at once:
+  // 16-CTA clusters took 12.3 us on the large-E routing against 7.6)
   const long long P = (long long)M * topk;
-  long long ca = (P + 4095) / 4096;
+  long long ca = (P + 2047) / 2048;
   if (ca < 1) ca = 1;
   if (ca > kMaxAlignCluster) ca = kMaxAlignCluster;
   int c = 1;
