@@ -260,6 +260,9 @@ __device__ __forceinline__ void run_group(const GroupCtx &g, int g0, int nvg) {
         if (q < C) sum += v[q];
       t[i] = sum;
     }
+    // this CTA reads no peer's partial t after this; the matching wait is
+    // at the end of the group
+    cluster_arrive_relaxed();
   }
   __syncthreads();
   if (g0 == 0) mbar_wait_for(&meta.bar, phase, abort, p.err, cfg.wait_limit_ns);
@@ -317,16 +320,11 @@ __device__ __forceinline__ void run_group(const GroupCtx &g, int g0, int nvg) {
       }
     }
   }
-  // Peers are done reading this CTA's partial t (and every thread with this
-  // group's shared memory) before the next group or block reuses it, or
-  // before the CTA exits.  Relaxed: nothing here needs this thread's
-  // global stores to have drained.
-  if (C > 1) {
-    cluster_arrive_relaxed();
-    cluster_wait();
-  } else {
-    __syncthreads();
-  }
+  // Peers are done reading this CTA's partial t (they arrived after their
+  // reads) and every thread with this group's shared memory before the next
+  // group or block reuses it, or before the CTA exits.
+  if (C > 1) cluster_wait();
+  __syncthreads();
 }
 
 // RV: elements of B per shared-memory vector (8 when rank % 8 == 0, else 4).
