@@ -120,54 +120,6 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     if (global_timer_ns() - t0 > kWaitTimeoutNs) return;
 }
 
-// Packed pairs of fp32 (f32x2) in a 64-bit register: the arithmetic runs two
-// lanes of a vector per instruction (fma.rn.f32x2).
-typedef unsigned long long f32x2;
-
-__device__ __forceinline__ f32x2 f2_pack(float lo, float hi) {
-  f32x2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ float f2_sum(f32x2 v) {
-  float lo, hi;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  return lo + hi;
-}
-// the two bf16 of a 32-bit word, widened (exactly) to fp32
-__device__ __forceinline__ f32x2 bf2_to_f2(uint32_t w) {
-  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-__device__ __forceinline__ f32x2 ffma2(f32x2 a, f32x2 b, f32x2 c) {
-  f32x2 d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-// one 16-byte vector of bf16 as four f32x2
-__device__ __forceinline__ void unpack_v(const uint4 v, f32x2 (&f)[4]) {
-  f[0] = bf2_to_f2(v.x);
-  f[1] = bf2_to_f2(v.y);
-  f[2] = bf2_to_f2(v.z);
-  f[3] = bf2_to_f2(v.w);
-}
-
-// c + sum_i a[i] * b[i] over one 16-byte vector of bf16 pairs: mixed
-// precision FMAs (bf16 operands, exact products, fp32 accumulation and
-// rounding), so neither operand is widened first.
-__device__ __forceinline__ float dot8_bf16_acc(const uint4 a, const uint4 b, float c) {
-  const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
-        "mov.b32 {al, ah}, %1;\n\t"
-        "mov.b32 {bl, bh}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, al, bl, %0;\n\t"
-        "fma.rn.f32.bf16 %0, ah, bh, %0;\n\t}"
-        : "+f"(c)
-        : "r"(wa[i]), "r"(wb[i]));
-  return c;
-}
-
 // Row sums over a group of G consecutive lanes (G a power of two up to 32),
 // each lane holding partial sums of the same V rows.  While a lane holds more
 // than one row, a step with lane distance d hands half of its rows to the
