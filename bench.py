@@ -661,8 +661,13 @@ def run_ours(args, world, rank, local, pg):
             host_pack[off:off + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).view(np.uint8).reshape(-1)))
         tdt = {"topk_ids": torch.int32, "mapping": torch.int32, "lora_ids": torch.int32, "x": torch.bfloat16,
                "y": torch.bfloat16, "w": torch.float32}
+        # three device buffers: in the pipelined mode step i + 1's inputs go
+        # up while step i computes and step i - 1's y comes back (with two, a
+        # buffer's upload would wait for its previous read-back, and the
+        # copies and calls would chain into one cycle per two steps)
+        NBUF = 3
         packs = []
-        for k in range(2):
+        for k in range(NBUF):
             dev_pack = torch.empty(total, dtype=torch.uint8, device=dev)
             v = {"pack": dev_pack}
             for name, (off, arr) in layout.items():
@@ -721,20 +726,21 @@ def run_ours(args, world, rank, local, pg):
         del g_e2e
         # Pipelined: the same copies and calls with the copies on their own
         # streams, so that step i + 1's inputs go up and step i - 1's y comes
-        # back while step i computes (two packed buffers and two pinned
-        # outputs alternate; a buffer is refilled only after its y has been
-        # read back).
+        # back while step i computes (three packed buffers and three pinned
+        # outputs rotate; a buffer is refilled only after its y has been read
+        # back).
         s_in = torch.cuda.Stream(device=dev)
         s_out = torch.cuda.Stream(device=dev)
-        out_hosts = [out_host, torch.empty(src.y_in.shape, dtype=torch.int16).pin_memory()]
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_cmp = [torch.cuda.Event() for _ in range(2)]
-        ev_free = [torch.cuda.Event() for _ in range(2)]
+        out_hosts = [out_host] + [torch.empty(src.y_in.shape, dtype=torch.int16).pin_memory()
+                                  for _ in range(NBUF - 1)]
+        ev_in = [torch.cuda.Event() for _ in range(NBUF)]
+        ev_cmp = [torch.cuda.Event() for _ in range(NBUF)]
+        ev_free = [torch.cuda.Event() for _ in range(NBUF)]
 
         def piped_step(i):
-            k = i % 2
+            k = i % NBUF
             v = packs[k]
-            if i >= 2:
+            if i >= NBUF:
                 s_in.wait_event(ev_free[k])
             with torch.cuda.stream(s_in):
                 v["pack"].copy_(host_pack, non_blocking=True)
