@@ -166,6 +166,31 @@ def test_fused_no_covered_pairs(path):
     assert err == 0 and np.array_equal(host_bf16_bits(y).reshape(inp.y_in.shape), inp.y_in)
 
 
+@pytest.mark.parametrize("shape", ["two_pairs_clusters", "one_pair"])
+def test_fused_stream_units_in_turn(shape):
+    """More aligned blocks than the streaming kernel's list builder counts in
+    one pass (1280): it takes the units in turn instead of the balanced list.
+    Two pairs per item over 4-CTA clusters (pairs beyond the (LoRA, expert)
+    pairs), and one pair per item (pairs no more than those).  Every element
+    against the oracle."""
+    if shape == "two_pairs_clusters":
+        w = gen.Workload("stream_in_turn_2", M=4096, K=128, N=128, E=64, topk=8, max_loras=2, num_active_loras=2,
+                         rank=16, block_size=16, mapping="uniform", experts="uniform", seed=5)
+    else:
+        w = gen.Workload("stream_in_turn_1", M=2048, K=64, N=64, E=1024, topk=8, max_loras=16, num_active_loras=16,
+                         rank=16, block_size=16, mapping="uniform", experts="uniform", seed=6)
+    plan = B.fused_plan(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size,
+                        path=B.PATH_CUDA_CORE_STREAM, sm_count=152, max_smem_per_block=232448)
+    assert plan["pairs_per_group"] == (2 if shape == "two_pairs_clusters" else 1), plan
+    inp = gen.make_inputs(w)
+    # the routing really has more blocks than one counting pass covers
+    per_slot = [np.bincount(inp.topk_ids.reshape(-1)[np.repeat(inp.token_lora_mapping, w.topk) == l],
+                            minlength=w.E) for l in inp.lora_ids]
+    blocks = sum(int(np.sum((c + w.block_size - 1) // w.block_size)) for c in per_slot)
+    assert blocks > 1280, blocks
+    run_and_compare_full(inp, B.PATH_CUDA_CORE_STREAM, add_inputs=True)
+
+
 @pytest.mark.parametrize("variant", [B.ALIGN_SMEM, B.ALIGN_GLOBAL, B.ALIGN_CLUSTER])
 def test_fused_after_either_align_variant(variant):
     inp = gen.make_inputs(gen.WORKLOADS["decode_gptoss_w2"])
