@@ -541,7 +541,8 @@ def kernel_name_of(B, w, args):
     name = {B.PATH_TCGEN05: "fused_tcgen05_kernel", B.PATH_CUDA_CORE_CLUSTER: "fused_cuda_core_kernel",
             B.PATH_CUDA_CORE_STREAM: "fused_cluster_stream_kernel"}[kernel]
     if args.naive:
-        name = ("fused_cluster_stream_kernel" if args.path == B.PATH_CUDA_CORE_STREAM else "fused_cuda_core_kernel") \
+        naive_path = B.fused_naive_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, args.slices, args.path)
+        name = ("fused_cluster_stream_kernel" if naive_path == B.PATH_CUDA_CORE_STREAM else "fused_cuda_core_kernel") \
             + " (naive block assignment)"
     return name
 
@@ -563,6 +564,16 @@ def config_entry(rig, counts, peak, tc_peak, seconds):
         align["align_us_cluster"] = rig.graph_time_us(lambda s: rig.align(s, B.ALIGN_CLUSTER), seconds)
         align["align_variant_auto"] = rig.auto_variant_name()
     step_us = rig.graph_time_us(lambda s: (rig.align(s) if not rig.args.naive else None, rig.fused(s)), seconds)
+    # Decode batches: the same batch through the naive entry point (no align,
+    # one work item per pair), the model's other way to run a small batch.
+    if not rig.args.naive and not uses_ex(rig.args) and w.M * w.topk <= 4096:
+        def naive(s):
+            B.moe_lora_fused_shrink_expand_naive(s["x"], s["a0"], s["b0"], s["y"], s["topk_ids"], s["mapping"],
+                                                 s["lora_ids"], w.max_loras, add_inputs=True, err_flag=rig.err,
+                                                 stream=rig.stream)
+        align["naive_step_us"] = rig.graph_time_us(naive, seconds)
+        align["naive_kernel"] = "fused_cluster_stream_kernel" if B.fused_naive_resolve_path(
+            w.M, w.topk, w.E, w.K, w.N, w.rank) == B.PATH_CUDA_CORE_STREAM else "fused_cuda_core_kernel"
     rig.check_err()
     gbs = counts["fused_bytes"] / (fused_us * 1e-6) / 1e9
     tflops = counts["flops"] / (fused_us * 1e-6) / 1e12

@@ -367,6 +367,17 @@ int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, 
                                 int num_active_loras, int block_size, int num_slices, int path);
 
 /*
+ * moe_lora_fused_naive_resolve_path -- the kernel a naive-assignment call
+ * (moe_lora_fused_shrink_expand_naive / _ex) with these sizes runs:
+ * MOE_LORA_PATH_CUDA_CORE_CLUSTER or MOE_LORA_PATH_CUDA_CORE_STREAM, or a
+ * negative moe_lora_status code if `path` (AUTO, CUDA_CORE, CUDA_CORE_CLUSTER
+ * or CUDA_CORE_STREAM) is not valid for these sizes.  Host only; no device is
+ * touched.
+ */
+int moe_lora_fused_naive_resolve_path(int M, int topk, int num_experts, int K, int N, int rank,
+                                      int num_slices, int path);
+
+/*
  * moe_lora_fused_plan -- the launch plan a plain fused call with these sizes
  * would use on a device with `sm_count` SMs and `max_smem_per_block` bytes of
  * opt-in shared memory per block.  Host arithmetic only; no device is

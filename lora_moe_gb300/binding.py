@@ -81,6 +81,8 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_fused_plan.argtypes = [I] * 12 + [P]
             L.moe_lora_fused_resolve_path.restype = I
             L.moe_lora_fused_resolve_path.argtypes = [I] * 10
+            L.moe_lora_fused_naive_resolve_path.restype = I
+            L.moe_lora_fused_naive_resolve_path.argtypes = [I] * 8
             _lib = L
     return _lib
 
@@ -208,6 +210,15 @@ def moe_lora_fused_shrink_expand(x, lora_a, lora_b, y, sorted_token_ids, expert_
         sorted_token_ids.shape[-1], expert_ids.shape[-1], int(bool(add_inputs)), path,
         _ptr(err_flag, torch.int32, "err_flag"), _stream(stream))
     _check(st, "moe_lora_fused_shrink_expand")
+
+
+def fused_naive_resolve_path(M, topk, num_experts, K, N, rank, num_slices=1, path=PATH_AUTO) -> int:
+    """The kernel a naive-assignment call with these sizes runs
+    (PATH_CUDA_CORE_CLUSTER or PATH_CUDA_CORE_STREAM)."""
+    v = lib().moe_lora_fused_naive_resolve_path(M, topk, num_experts, K, N, rank, num_slices, path)
+    if v < 0:
+        raise MoeLoraError(-v, "moe_lora_fused_naive_resolve_path")
+    return v
 
 
 def fused_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices=1,

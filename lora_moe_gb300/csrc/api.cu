@@ -409,6 +409,27 @@ static int resolve_path_query(int M, int topk, int num_experts, int K, int N, in
   return resolve_path(f, path, max_smem);
 }
 
+int moe_lora_fused_naive_resolve_path(int M, int topk, int num_experts, int K, int N, int rank, int num_slices,
+                                      int path) {
+  if (M < 0 || topk < 1 || num_experts < 1 || K < 8 || N < 8 || rank < 1 || num_slices < 1 ||
+      num_slices > kMaxSlices)
+    return -MOE_LORA_ERR_INVALID_ARG;
+  if (path != MOE_LORA_PATH_AUTO && path != MOE_LORA_PATH_CUDA_CORE && path != MOE_LORA_PATH_CUDA_CORE_CLUSTER &&
+      path != MOE_LORA_PATH_CUDA_CORE_STREAM)
+    return -MOE_LORA_ERR_INVALID_ARG;
+  if (rank > kMaxRank || rank % 4 != 0 || !path_takes_rank(path, rank)) return -MOE_LORA_ERR_UNSUPPORTED;
+  FusedArgs f = {};
+  f.M = M;
+  f.topk = topk;
+  f.num_experts = num_experts;
+  f.K = K;
+  f.N = N;
+  f.rank = rank;
+  f.num_slices = num_slices;
+  f.block_size = 16;
+  return resolve_naive_path(f, path);
+}
+
 int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, int rank, int num_active_loras,
                                 int block_size, int num_slices, int path) {
   return resolve_path_query(M, topk, num_experts, K, N, rank, num_active_loras, block_size, num_slices, path,

@@ -196,6 +196,22 @@ def test_fused_resolve_path():
     assert R(16, 8, 128, 2048, 1536, 16, 2, 16, 1, 9) == -1
 
 
+def test_naive_resolve_path():
+    """The naive assignment's kernel: the streaming kernel when the pairs'
+    adapters exceed 48 MB (gpt-oss-shaped w2 decode), else the
+    one-cluster-per-pair kernel (Qwen3-shaped decode); forced paths kept."""
+    R = B.lib().moe_lora_fused_naive_resolve_path
+    # (M, topk, E, K, N, rank, num_slices, path)
+    assert R(64, 4, 128, 2880, 2880, 64, 1, 0) == 4
+    assert R(16, 8, 128, 2048, 1536, 16, 1, 0) == 3
+    assert R(16, 8, 128, 2048, 1536, 16, 1, 1) == 3          # CUDA_CORE -> cluster
+    assert R(16, 8, 128, 2048, 1536, 16, 1, 4) == 4
+    assert R(16, 8, 128, 2048, 1536, 24, 1, 4) == -2         # streaming: ranks 8, 16, 32, 64, 128
+    assert R(16, 8, 128, 2048, 1536, 16, 1, 2) == -1         # no tensor-core naive path
+    assert R(16, 8, 128, 2048, 1536, 16, 5, 0) == -1         # too many slices
+    assert B.fused_naive_resolve_path(64, 4, 128, 2880, 2880, 64) == B.PATH_CUDA_CORE_STREAM
+
+
 def test_align_resolve_variant():
     R = B.lib().moe_lora_align_resolve_variant
     assert R(16, 8, 128, 0) in (1, 2, 3)          # AUTO resolves to a concrete variant
