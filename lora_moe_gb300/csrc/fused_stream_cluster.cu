@@ -938,18 +938,23 @@ int launch_with(const FusedArgs &f, const CsCfg &cfg, long long G, cudaStream_t 
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = cfg.smem_bytes;
   lc.stream = stream;
-  // Launched after the align kernel completes (no programmatic dependent
-  // launch): the grid is every cluster that fits on an idle GPU, and clusters
-  // launched early beside the align's CTAs could not all be placed -- the
-  // rest would run as a second wave, each with a full share of the units.
-  // (griddepcontrol.wait in the kernel is then a no-op.)
-  cudaLaunchAttribute attr[1];
+  // Single-CTA clusters (one pair per item, at most one item per CTA on
+  // decode batches) are launched as programmatic dependents: a CTA may start
+  // while the kernel before it finishes and waits for it with
+  // griddepcontrol.wait before reading any input (gpt-oss w2 decode step
+  // 39.1 -> 37.4 us).  Larger clusters are launched after it completes: the
+  // grid is every cluster that fits on an idle GPU, and clusters launched
+  // early beside the align's CTAs could not all be placed -- the rest would
+  // run as a second wave, each with a full share of the units.
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cfg.C;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = cfg.C == 1 ? 2 : 1;
   return cudaLaunchKernelEx(&lc, fused_cluster_stream_kernel<NAIVE, LG_VR, NPG>, maps, f, cfg) == cudaSuccess
              ? 0
              : MOE_LORA_ERR_LAUNCH;
