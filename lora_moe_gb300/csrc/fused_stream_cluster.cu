@@ -213,23 +213,28 @@ __device__ void build_item_list(CsMeta &meta, const FusedArgs &p, int nact, int 
       const int l = meta.lids[z];
       const int32_t *ids =
           p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + (size_t)(b - meta.prefix[z]) * p.block_size;
+      // A block's real pairs come first and padding fills its tail (the
+      // align's layout), so the count stops at the first padding entry:
+      // decode blocks need one 16-byte read.
       int n = 0;
       if ((reinterpret_cast<uintptr_t>(ids) & 15) == 0 && (p.block_size & 3) == 0) {
-#pragma unroll 4
         for (int k = 0; k < p.block_size; k += 4) {
           const int4 v = __ldg(reinterpret_cast<const int4 *>(ids + k));
-          n += (v.x >= 0 && v.x < P) + (v.y >= 0 && v.y < P) + (v.z >= 0 && v.z < P) + (v.w >= 0 && v.w < P);
+          const int c4 = (v.x >= 0 && v.x < P) + (v.y >= 0 && v.y < P) + (v.z >= 0 && v.z < P) + (v.w >= 0 && v.w < P);
+          n += c4;
+          if (c4 < 4) break;
         }
       } else {
-#pragma unroll 8
         for (int k = 0; k < p.block_size; ++k) {
           const int f = __ldg(ids + k);
-          n += (f >= 0 && f < P) ? 1 : 0;
+          if (f < 0 || f >= P) break;
+          ++n;
         }
       }
       nbk[i] = n;
-      cnt[NPG - 1] += n / NPG;
-      if (n % NPG) cnt[n % NPG - 1] += 1;
+      // (unrolled selects, not an index: the counts stay in registers)
+#pragma unroll
+      for (int k = 0; k < NPG; ++k) cnt[k] += (k == NPG - 1 ? n / NPG : 0) + (n % NPG == k + 1 ? 1 : 0);
     }
   }
   // exclusive scan of the counts over the threads (block order)
@@ -277,8 +282,12 @@ __device__ void build_item_list(CsMeta &meta, const FusedArgs &p, int nact, int 
     const int n = nbk[i], b = b0 + i;
     const int groups = n / NPG + (n % NPG ? 1 : 0);
     for (int j = 0; j < groups; ++j) {
-      const int k = (j < n / NPG ? NPG : n % NPG) - 1;
-      const long long idx0 = (long long)(off[k] + run[k]++) * S;
+      const int kk = (j < n / NPG ? NPG : n % NPG) - 1;
+      int rank_k = 0;
+#pragma unroll
+      for (int k = 0; k < NPG; ++k)
+        if (k == kk) rank_k = off[k] + run[k]++;
+      const long long idx0 = (long long)rank_k * S;
       for (int s = 0; s < S; ++s) {
         const long long idx = idx0 + s, round = idx / G, pos = idx - round * G;
         if (((round & 1) ? G - 1 - pos : pos) == g) meta.list[round] = (b << 8) | (j << 2) | s;
