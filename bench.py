@@ -138,12 +138,13 @@ def algorithmic_counts(inp: gen.Inputs, slices=1, per_pair_x=False, routed_weigh
 # and kernel; profiles/ holds each capture's summary and command.  An entry
 # must go when its kernel changes.
 NCU_TRAFFIC = {
-    ("decode_qwen3_w13", "fused_cuda_core_kernel"): 5573632,      # fused_cuda_core_decode_qwen3_w13.md
+    ("decode_qwen3_w13", "fused_cuda_core_kernel"): 5580032,      # fused_cuda_core_decode_qwen3_w13.md
     ("decode_gptoss_w2", "fused_tcgen05_kernel"): 170909184,      # fused_tcgen05_decode_gptoss_w2.md
-    ("decode_gptoss_w2", "fused_cluster_stream_kernel"): 155517696,  # fused_cluster_stream_decode_gptoss_w2.md
+    ("decode_gptoss_w2", "fused_cluster_stream_kernel"): 155413504,  # fused_cluster_stream_decode_gptoss_w2.md
     ("large_e_l1", "fused_tcgen05_kernel"): 1080333056,           # fused_tcgen05_large_e_l1.md
     # the same active work as large_e_l1 (the inactive slots are never read)
     ("large_e_nact1", "fused_tcgen05_kernel"): 1080333056,        # fused_tcgen05_large_e_l1.md
+    ("large_e_nact4", "fused_tcgen05_kernel"): 3439547904,        # fused_tcgen05_large_e_nact4_traffic.md
     ("large_e_nact8", "fused_tcgen05_kernel"): 6153373440,        # fused_tcgen05_large_e_nact8_traffic.md
     ("prefill_mixtral_w13_m2048", "fused_tcgen05_kernel"): 468284416,  # fused_tcgen05_prefill_mixtral_w13_m2048.md
     ("prefill_mixtral_w13", "fused_tcgen05_kernel"): 2211975168,  # fused_tcgen05_prefill_mixtral_w13_traffic.md
