@@ -213,22 +213,18 @@ __device__ void build_item_list(CsMeta &meta, const FusedArgs &p, int nact, int 
       const int l = meta.lids[z];
       const int32_t *ids =
           p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + (size_t)(b - meta.prefix[z]) * p.block_size;
-      // A block's real pairs come first and padding fills its tail (the
-      // align's layout), so the count stops at the first padding entry:
-      // decode blocks need one 16-byte read.
+      // Every entry is counted (the count does not rely on a block's real
+      // pairs preceding its padding); 16-byte reads where aligned.
       int n = 0;
       if ((reinterpret_cast<uintptr_t>(ids) & 15) == 0 && (p.block_size & 3) == 0) {
         for (int k = 0; k < p.block_size; k += 4) {
           const int4 v = __ldg(reinterpret_cast<const int4 *>(ids + k));
-          const int c4 = (v.x >= 0 && v.x < P) + (v.y >= 0 && v.y < P) + (v.z >= 0 && v.z < P) + (v.w >= 0 && v.w < P);
-          n += c4;
-          if (c4 < 4) break;
+          n += (v.x >= 0 && v.x < P) + (v.y >= 0 && v.y < P) + (v.z >= 0 && v.z < P) + (v.w >= 0 && v.w < P);
         }
       } else {
         for (int k = 0; k < p.block_size; ++k) {
           const int f = __ldg(ids + k);
-          if (f < 0 || f >= P) break;
-          ++n;
+          n += (f >= 0 && f < P) ? 1 : 0;
         }
       }
       nbk[i] = n;
