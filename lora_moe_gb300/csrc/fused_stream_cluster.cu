@@ -16,23 +16,29 @@
 // At decode sizes a block holds one or a few real pairs, so the work is a
 // skinny GEMV bound by streaming A[l,e] (r x K) and B[l,e] (N x r) from HBM.
 // Design:
-//   * a cluster of C CTAs (one per SM) works on one unit (block, slice) at a
-//     time; CTA c owns the K columns [k_lo(c), k_hi(c)) of the shrink and the
-//     output rows [n_lo(c), n_hi(c)) of the expand, so every adapter byte is
-//     read once, by one CTA.  Persistent clusters take units strided over the
-//     grid (vLLM PR #32005: the work list covers the active LoRAs only).
-//   * a producer warp streams each unit's share through a ring of stages:
-//     A boxes of r rows x kc columns by TMA (3-D tensor map), with the kc
-//     columns of the pairs' x rows by bulk copies beside them; then B rows by
-//     bulk copies, with the matching y_in pieces.  It runs ahead across units
-//     as far as the ring allows.
-//   * eight consumer warps accumulate each CTA's partial t over its K columns
-//     in registers, push the partial (fp32) into every peer's shared memory
-//     with st.async (completion counted on the peer's mbarrier), sum the C
-//     partials in rank order (deterministic) and expand their N rows.  t never
-//     leaves shared memory or registers.
-//   * a unit with more than NPG real pairs is applied NPG pairs at a time
-//     (its adapters re-streamed, from L2).
+//   * work items are NPG pairs of one unit (block, slice): NPG = 1 for the
+//     naive assignment and for decode batches (a block's second pair re-reads
+//     the block's adapters, mostly from L2), NPG = 2 otherwise.
+//   * a cluster of C CTAs (C = 1 with NPG = 1, up to 4 with NPG = 2) works on
+//     one item at a time; CTA c owns the K columns [k_lo(c), k_hi(c)) of the
+//     shrink and the output rows [n_lo(c), n_hi(c)) of the expand, so every
+//     adapter byte of the item is read once, by one CTA.
+//   * the items of aligned blocks come from a balanced list that every
+//     cluster builds the same way (each block's real pairs counted, the items
+//     ordered by pair count and dealt to the clusters in a snake); beyond
+//     what the list covers, units are taken in turn (vLLM PR #32005: the work
+//     list covers the active LoRAs only).
+//   * two producer warps stream each item's share through a ring of 16 KB
+//     stages: A boxes of r rows x kc columns by TMA (3-D tensor map), with
+//     the kc columns of the pairs' x rows by bulk copies beside them; then B
+//     rows by bulk copies, with the matching y_in pieces.  They run ahead
+//     across items as far as the ring allows.
+//   * eight consumer warps copy each stage to registers and hand it back,
+//     then accumulate each CTA's partial t over its K columns; with C > 1 the
+//     partial (fp32) goes into every peer's shared memory by st.async
+//     (completion counted on the peer's mbarrier) and each CTA sums the C
+//     partials in rank order (deterministic).  They then expand the item's
+//     N rows.  t never leaves shared memory or registers.
 // Every wait is bounded.
 #include <cooperative_groups.h>
 #include <cuda.h>
