@@ -75,7 +75,9 @@ typedef enum {
 #define MOE_LORA_DEVERR_EXPERT_ID 0x1   /* topk_ids / expert_ids entry outside [0, num_experts) */
 #define MOE_LORA_DEVERR_LORA_ID 0x2     /* lora_ids entry outside [0, max_loras) */
 #define MOE_LORA_DEVERR_CAPACITY 0x4    /* align output larger than max_num_tokens_padded */
-#define MOE_LORA_DEVERR_PAIR_ID 0x8     /* sorted_token_ids entry neither a pair nor the sentinel */
+#define MOE_LORA_DEVERR_PAIR_ID 0x8     /* sorted_token_ids entry neither a pair nor the sentinel
+                                           (the streaming kernel also flags a block whose pairs
+                                           do not all precede its sentinels) */
 #define MOE_LORA_DEVERR_TIMEOUT 0x10    /* an on-chip wait gave up (a bounded wait ran out) */
 
 /* Align variants (moe_lora_align `variant`). */

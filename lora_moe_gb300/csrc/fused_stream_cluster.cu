@@ -219,18 +219,26 @@ __device__ void build_item_list(CsMeta &meta, const FusedArgs &p, int nact, int 
       const int l = meta.lids[z];
       const int32_t *ids =
           p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + (size_t)(b - meta.prefix[z]) * p.block_size;
-      // Every entry is counted (the count does not rely on a block's real
-      // pairs preceding its padding); 16-byte reads where aligned.
+      // In the align's layout a block's real pairs come first and the
+      // sentinel fills its tail, so the count stops at the first entry that
+      // is not a pair: a decode block takes one 16-byte read.  (The producers
+      // flag a block that breaks this layout.)
       int n = 0;
       if ((reinterpret_cast<uintptr_t>(ids) & 15) == 0 && (p.block_size & 3) == 0) {
         for (int k = 0; k < p.block_size; k += 4) {
           const int4 v = __ldg(reinterpret_cast<const int4 *>(ids + k));
-          n += (v.x >= 0 && v.x < P) + (v.y >= 0 && v.y < P) + (v.z >= 0 && v.z < P) + (v.w >= 0 && v.w < P);
+          const unsigned m4 = (v.x >= 0 && v.x < P) | (v.y >= 0 && v.y < P) << 1 | (v.z >= 0 && v.z < P) << 2 |
+                              (v.w >= 0 && v.w < P) << 3;
+          if (m4 & (m4 + 1u)) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);   // a pair after a sentinel
+          const int c4 = __popc(m4);
+          n += c4;
+          if (c4 < 4) break;
         }
       } else {
         for (int k = 0; k < p.block_size; ++k) {
           const int f = __ldg(ids + k);
-          n += (f >= 0 && f < P) ? 1 : 0;
+          if (f < 0 || f >= P) break;
+          ++n;
         }
       }
       nbk[i] = n;
@@ -482,11 +490,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         le = l * E + e;
         const int32_t *ids = p.sorted_token_ids + (size_t)l * p.max_num_tokens_padded + (size_t)b * p.block_size;
+        bool gap = false;   // an entry that is not a pair has been seen
         for (int i0 = 0; i0 < p.block_size; i0 += 32) {
           const int f = i0 + lane < p.block_size ? __ldg(ids + i0 + lane) : P;
           const bool real = f >= 0 && f < P;
           if ((f < 0 || f > P) && pw == 0 && c == 0 && s == 0) flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
           const unsigned bal = __ballot_sync(0xffffffffu, real);
+          // the align's layout: real pairs first, then the sentinel (the
+          // balanced list counts on it)
+          if (((gap && bal) || (bal & (bal + 1u))) && lead && pw == 0 && c == 0 && s == 0)
+            flag_error(p.err, MOE_LORA_DEVERR_PAIR_ID);
+          gap = gap || bal != 0xffffffffu;
           if (real) pf[np + __popc(bal & ((1u << lane) - 1u))] = f;
           np += __popc(bal);
         }

@@ -191,6 +191,40 @@ def test_fused_stream_units_in_turn(shape):
     run_and_compare_full(inp, B.PATH_CUDA_CORE_STREAM, add_inputs=True)
 
 
+def test_fused_stream_flags_out_of_layout_block():
+    """A block whose pair follows a sentinel (a layout moe_lora_align never
+    writes): the streaming kernel's balanced list counts each block's pairs up
+    to its first sentinel, so it flags the block (DEVERR_PAIR_ID) instead of
+    dropping the pair silently."""
+    import torch
+    from helpers import DeviceInputs
+    w = gen.Workload("stream_layout", M=16, K=64, N=64, E=64, topk=2, max_loras=2, num_active_loras=2, rank=16,
+                     block_size=16, mapping="uniform", experts="uniform", seed=3)
+    assert B.fused_plan(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, w.block_size,
+                        path=B.PATH_CUDA_CORE_STREAM, sm_count=152, max_smem_per_block=232448)["pairs_per_group"] == 1
+    inp = gen.make_inputs(w)
+    d = DeviceInputs(inp)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.moe_lora_align(d.topk_ids, d.mapping, d.lora_ids, w.E, w.max_loras, w.block_size, d.buf.sorted_token_ids,
+                     d.buf.expert_ids, d.buf.num_tokens_post_padded, workspace=d.buf.workspace, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    # the first block of the first slot: swap its first pair with the sentinel after it
+    l = int(inp.lora_ids[0])
+    row = d.buf.sorted_token_ids[l]
+    sentinel = w.M * w.topk
+    blk = row[:w.block_size].clone()
+    n_real = int((blk < sentinel).sum().item())
+    assert 1 <= n_real < w.block_size
+    row[n_real - 1], row[n_real] = sentinel, int(blk[n_real - 1].item())
+    y = d.y_in.clone()
+    B.moe_lora_fused_shrink_expand(d.x, d.a, d.b, y, d.buf.sorted_token_ids, d.buf.expert_ids,
+                                   d.buf.num_tokens_post_padded, d.lora_ids, w.topk, w.block_size, add_inputs=True,
+                                   path=B.PATH_CUDA_CORE_STREAM, err_flag=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & B.DEVERR_PAIR_ID
+
+
 @pytest.mark.parametrize("variant", [B.ALIGN_SMEM, B.ALIGN_GLOBAL, B.ALIGN_CLUSTER])
 def test_fused_after_either_align_variant(variant):
     inp = gen.make_inputs(gen.WORKLOADS["decode_gptoss_w2"])
