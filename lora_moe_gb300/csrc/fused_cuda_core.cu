@@ -522,12 +522,18 @@ bool layout(const FusedArgs &f, const DeviceInfo &dev, int C, int pg, CcCfg *cfg
 // Spread a block's adapter bytes over up to 16 CTAs: at least ~12 KB each
 // (so that each CTA is worth its launch, up to 8 CTAs) and at most ~48 KB each
 // (so that several CTAs share an SM); more CTAs if shared memory demands it.
+// Blocks of the align output (one cluster per block, grid capped at the
+// resident clusters) whose adapters want more than 8 CTAs take clusters of
+// 12 (non-portable): measured on the Qwen3-shaped w13 decode 7.5 against
+// 8.2 us with 8 (10: 8.5, 16: 11.4), on the gpt-oss-shaped w2 decode 103
+// against 123 us.  The naive assignment (a cluster per pair, several waves)
+// keeps 8 (12: 8.5 against 7.6 us on Qwen3).
 // pg: the preferred pairs per group; smaller groups are tried if it does not fit.
-int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, int pg, CcCfg *cfg) {
+int pick_cfg(const FusedArgs &f, const DeviceInfo &dev, int pg, bool per_block, CcCfg *cfg) {
   const long long item_bytes = (long long)(f.K + f.N) * f.rank * 2;
   const long long lo = (item_bytes + 48 * 1024 - 1) / (48 * 1024);
   long long hi = (item_bytes + 12 * 1024 - 1) / (12 * 1024);
-  if (hi > 8) hi = 8;
+  if (hi > 8) hi = per_block && f.K / 8 >= 12 && f.N / 8 >= 12 ? 12 : 8;
   long long want = lo > hi ? lo : hi;
   const long long cmax = std::min<long long>(kMaxCluster, std::min(f.K / 8, f.N / 8));
   if (want > cmax) want = cmax;
@@ -630,7 +636,7 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
   // Room for groups of eight pairs where it fits (blocks with more than two
   // real pairs run eight at a time; the others the two-pair body).
   CcCfg cfg;
-  if (int st = pick_cfg(f, dev, 8, &cfg)) return st;
+  if (int st = pick_cfg(f, dev, 8, true, &cfg)) return st;
   long long per_slot = pairs / f.block_size + (pairs < f.num_experts ? pairs : f.num_experts);
   if (per_slot > f.max_num_m_blocks) per_slot = f.max_num_m_blocks;
   // Blocks a slot really has are usually far fewer than that bound: the grid
@@ -655,7 +661,7 @@ int launch_fused_cuda_core(const FusedArgs &f, cudaStream_t stream) {
 int plan_fused_cuda_core(const FusedArgs &f, const DeviceInfo &dev, FusedPlan *out) {
   if (f.block_size > kMaxBlock) return MOE_LORA_ERR_UNSUPPORTED;
   CcCfg cfg;
-  if (int st = pick_cfg(f, dev, 8, &cfg)) return st;
+  if (int st = pick_cfg(f, dev, 8, true, &cfg)) return st;
   out->kernel = MOE_LORA_PATH_CUDA_CORE_CLUSTER;
   out->grid = 0;   // capped at run time by the clusters that can be resident at once
   out->threads = kThreads;
@@ -670,7 +676,7 @@ int launch_fused_naive(const FusedArgs &f, cudaStream_t stream, unsigned long lo
   DeviceInfo dev;
   if (int st = current_device_info(&dev)) return st;
   CcCfg cfg;
-  if (int st = pick_cfg(f, dev, 1, &cfg)) return st;
+  if (int st = pick_cfg(f, dev, 1, false, &cfg)) return st;
   if (wait_limit_ns) cfg.wait_limit_ns = wait_limit_ns;
   cfg.withhold_b = withhold_b;
   // grid (C, slices, pairs), as the one-program-per-pair grid of the naive

@@ -25,7 +25,7 @@ PINNED = {
     "prefill_mixtral_w13": (B.PATH_TCGEN05, 10, 4, 6, 1, 256),
     "large_e_nact1": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
     "large_e_nact8": (B.PATH_TCGEN05, 4, 1, 2, 1, 256),
-    "decode_qwen3_w13": (B.PATH_CUDA_CORE_CLUSTER, 8, 8),
+    "decode_qwen3_w13": (B.PATH_CUDA_CORE_CLUSTER, 12, 8),
     "tiny": (B.PATH_CUDA_CORE_CLUSTER, 1, 8),
 }
 

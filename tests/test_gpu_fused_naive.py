@@ -139,10 +139,14 @@ def test_naive_disabled_adapter_and_bad_ids(path):
 
 
 @pytest.mark.parametrize("opt", ["plain", "w2_per_pair_weighted", "three_slices_offset_per_pair"])
-@pytest.mark.parametrize("name", ["decode_qwen3_w13", "decode_gptoss_w2"])
+@pytest.mark.parametrize("name", ["tiny", "decode_qwen3_w13", "decode_gptoss_w2"])
 def test_naive_equals_sorted_cluster_bits(name, opt):
     """Naive and sorted assignment run the same per-pair arithmetic on the
-    cluster kernel: their outputs agree bit for bit."""
+    cluster kernel: with the same cluster size their outputs agree bit for
+    bit.  Blocks whose adapters exceed 8 x 12 KB take 12-CTA clusters on the
+    sorted path and 8 on the naive one (the K and N slices, hence the fp32
+    summation order, differ): there both stay within the oracle's tolerance
+    of each other."""
     import torch
     from helpers import dev_bf16, dev_i32
     w = gen.WORKLOADS[name]
@@ -161,4 +165,9 @@ def test_naive_equals_sorted_cluster_bits(name, opt):
         buf.sorted_token_ids, buf.expert_ids, buf.num_tokens_post_padded, lora_ids, w.topk, w.block_size,
         topk_weights=wts, x_per_pair=ex.x_per_pair, y_offset=ex.y_offset, path=B.PATH_CUDA_CORE_CLUSTER)
     torch.cuda.synchronize()
-    assert torch.equal(y.view(torch.int16), y_naive.view(torch.int16))
+    twelve = (w.K + w.N) * w.rank * 2 > 8 * 12 * 1024 and w.K // 8 >= 12 and w.N // 8 >= 12
+    if not twelve:
+        assert torch.equal(y.view(torch.int16), y_naive.view(torch.int16))
+    else:
+        a, b = y.float(), y_naive.float()
+        assert torch.all((a - b).abs() <= 1e-2 + 1e-2 * b.abs())
