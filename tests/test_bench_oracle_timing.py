@@ -131,6 +131,9 @@ def test_default_workload_and_config_list():
     finally:
         sys.argv = old
     assert a.workload == "large_e_nact8" and a.configs == "all" and a.min_regions >= 5
+    # with no flags the run finishes in about a minute: 200 steps of the
+    # 1.2 ms headline step per timed region, at least 3 warm-up steps
+    assert a.gpus == 1 and 3 <= a.warmup <= 100 and 1 <= a.steps <= 1000
 
 
 @pytest.mark.parametrize("v,name", [(0, None), (1, "smem (forced)"), (2, "global (forced)"), (3, "cluster (forced)")])
