@@ -59,7 +59,7 @@ namespace {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kProducerWarps = 2;           // stage it is issued by producer warp it % 2
+constexpr int kProducerWarps = 2;           // ring stage st is filled by producer warp st % 2
 constexpr int kThreads = kConsumers + kProducerWarps * 32;
 constexpr int kNPG = 2;                     // most pairs a work item holds (NPG: 1 or kNPG)
 constexpr int kDesc = 8;                    // work-item descriptors in flight
