@@ -542,7 +542,8 @@ def kernel_name_of(B, w, args):
     name = {B.PATH_TCGEN05: "fused_tcgen05_kernel", B.PATH_CUDA_CORE_CLUSTER: "fused_cuda_core_kernel",
             B.PATH_CUDA_CORE_STREAM: "fused_cluster_stream_kernel"}[kernel]
     if args.naive:
-        naive_path = B.fused_naive_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, args.slices, args.path)
+        naive_path = B.fused_naive_resolve_path(w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras, args.slices,
+                                                args.path)
         name = ("fused_cluster_stream_kernel" if naive_path == B.PATH_CUDA_CORE_STREAM else "fused_cuda_core_kernel") \
             + " (naive block assignment)"
     return name
@@ -574,7 +575,8 @@ def config_entry(rig, counts, peak, tc_peak, seconds):
                                                  stream=rig.stream)
         align["naive_step_us"] = rig.graph_time_us(naive, seconds)
         align["naive_kernel"] = "fused_cluster_stream_kernel" if B.fused_naive_resolve_path(
-            w.M, w.topk, w.E, w.K, w.N, w.rank) == B.PATH_CUDA_CORE_STREAM else "fused_cuda_core_kernel"
+            w.M, w.topk, w.E, w.K, w.N, w.rank, w.num_active_loras) == B.PATH_CUDA_CORE_STREAM \
+            else "fused_cuda_core_kernel"
     rig.check_err()
     gbs = counts["fused_bytes"] / (fused_us * 1e-6) / 1e9
     tflops = counts["flops"] / (fused_us * 1e-6) / 1e12

@@ -377,7 +377,7 @@ int moe_lora_fused_resolve_path(int M, int topk, int num_experts, int K, int N, 
  * touched.
  */
 int moe_lora_fused_naive_resolve_path(int M, int topk, int num_experts, int K, int N, int rank,
-                                      int num_slices, int path);
+                                      int num_active_loras, int num_slices, int path);
 
 /*
  * moe_lora_fused_plan -- the launch plan a plain fused call with these sizes

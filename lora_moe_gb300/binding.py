@@ -82,7 +82,7 @@ def lib() -> ctypes.CDLL:
             L.moe_lora_fused_resolve_path.restype = I
             L.moe_lora_fused_resolve_path.argtypes = [I] * 10
             L.moe_lora_fused_naive_resolve_path.restype = I
-            L.moe_lora_fused_naive_resolve_path.argtypes = [I] * 8
+            L.moe_lora_fused_naive_resolve_path.argtypes = [I] * 9
             _lib = L
     return _lib
 
@@ -212,10 +212,10 @@ def moe_lora_fused_shrink_expand(x, lora_a, lora_b, y, sorted_token_ids, expert_
     _check(st, "moe_lora_fused_shrink_expand")
 
 
-def fused_naive_resolve_path(M, topk, num_experts, K, N, rank, num_slices=1, path=PATH_AUTO) -> int:
+def fused_naive_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, num_slices=1, path=PATH_AUTO) -> int:
     """The kernel a naive-assignment call with these sizes runs
     (PATH_CUDA_CORE_CLUSTER or PATH_CUDA_CORE_STREAM)."""
-    v = lib().moe_lora_fused_naive_resolve_path(M, topk, num_experts, K, N, rank, num_slices, path)
+    v = lib().moe_lora_fused_naive_resolve_path(M, topk, num_experts, K, N, rank, num_active_loras, num_slices, path)
     if v < 0:
         raise MoeLoraError(-v, "moe_lora_fused_naive_resolve_path")
     return v

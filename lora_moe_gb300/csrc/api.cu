@@ -409,10 +409,10 @@ static int resolve_path_query(int M, int topk, int num_experts, int K, int N, in
   return resolve_path(f, path, max_smem);
 }
 
-int moe_lora_fused_naive_resolve_path(int M, int topk, int num_experts, int K, int N, int rank, int num_slices,
-                                      int path) {
-  if (M < 0 || topk < 1 || num_experts < 1 || K < 8 || N < 8 || rank < 1 || num_slices < 1 ||
-      num_slices > kMaxSlices)
+int moe_lora_fused_naive_resolve_path(int M, int topk, int num_experts, int K, int N, int rank,
+                                      int num_active_loras, int num_slices, int path) {
+  if (M < 0 || topk < 1 || num_experts < 1 || K < 8 || N < 8 || rank < 1 || num_active_loras < 0 ||
+      num_slices < 1 || num_slices > kMaxSlices)
     return -MOE_LORA_ERR_INVALID_ARG;
   if (path != MOE_LORA_PATH_AUTO && path != MOE_LORA_PATH_CUDA_CORE && path != MOE_LORA_PATH_CUDA_CORE_CLUSTER &&
       path != MOE_LORA_PATH_CUDA_CORE_STREAM)
@@ -425,8 +425,9 @@ int moe_lora_fused_naive_resolve_path(int M, int topk, int num_experts, int K, i
   f.K = K;
   f.N = N;
   f.rank = rank;
+  f.num_active_loras = num_active_loras;
   f.num_slices = num_slices;
-  f.block_size = 16;
+  f.block_size = 16;   // (no blocks under the naive assignment)
   return resolve_naive_path(f, path);
 }
 

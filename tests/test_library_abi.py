@@ -201,15 +201,16 @@ def test_naive_resolve_path():
     adapters exceed 48 MB (gpt-oss-shaped w2 decode), else the
     one-cluster-per-pair kernel (Qwen3-shaped decode); forced paths kept."""
     R = B.lib().moe_lora_fused_naive_resolve_path
-    # (M, topk, E, K, N, rank, num_slices, path)
-    assert R(64, 4, 128, 2880, 2880, 64, 1, 0) == 4
-    assert R(16, 8, 128, 2048, 1536, 16, 1, 0) == 3
-    assert R(16, 8, 128, 2048, 1536, 16, 1, 1) == 3          # CUDA_CORE -> cluster
-    assert R(16, 8, 128, 2048, 1536, 16, 1, 4) == 4
-    assert R(16, 8, 128, 2048, 1536, 24, 1, 4) == -2         # streaming: ranks 8, 16, 32, 64, 128
-    assert R(16, 8, 128, 2048, 1536, 16, 1, 2) == -1         # no tensor-core naive path
-    assert R(16, 8, 128, 2048, 1536, 16, 5, 0) == -1         # too many slices
-    assert B.fused_naive_resolve_path(64, 4, 128, 2880, 2880, 64) == B.PATH_CUDA_CORE_STREAM
+    # (M, topk, E, K, N, rank, num_active_loras, num_slices, path)
+    assert R(64, 4, 128, 2880, 2880, 64, 6, 1, 0) == 4
+    assert R(64, 4, 128, 2880, 2880, 64, 129, 1, 0) == 3      # more slots than the streaming list indexes
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 1, 0) == 3
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 1, 1) == 3        # CUDA_CORE -> cluster
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 1, 4) == 4
+    assert R(16, 8, 128, 2048, 1536, 24, 2, 1, 4) == -2       # streaming: ranks 8, 16, 32, 64, 128
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 1, 2) == -1       # no tensor-core naive path
+    assert R(16, 8, 128, 2048, 1536, 16, 2, 5, 0) == -1       # too many slices
+    assert B.fused_naive_resolve_path(64, 4, 128, 2880, 2880, 64, 6) == B.PATH_CUDA_CORE_STREAM
 
 
 def test_align_resolve_variant():
